@@ -1,0 +1,556 @@
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas under torchrun).
+
+Headline (the JSON line's metric/value): paged decode attention, KV-read GB/s, on the
+decode-only Qwen3-235B-like layer: 256 sequences, context U[2000, 3000], 64 query / 4 KV
+heads, head_dim 128, block size 16, shuffled blocks in a pool 1.2x the need. One step is one
+pass of the hot path over that batch: batch_classify_reorder, kv_cache_write of the 256 new
+tokens, paged_decode_attn. value = KV bytes the decode reads / step time.
+
+Also reported on the same line: the mixed-batch step (Llama-3.1-70B-like: 192 decode, 8 extend
+x 512 over 4k-32k cached, 4 prefill of 2k-8k, random arrival order) in tokens/s; prefill and
+long-context extend TFLOP/s; KV write + per-layer pack GB/s over 80 layers of a 10k-token
+prompt; the roofline of the dominant kernel; and the CPU oracle timed on a bounded sample.
+
+--impl reference times the CPU oracle itself (the only reference implementation of this
+method) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pkv_workloads import gen  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sust": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "paged_kv_attention_reshape_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of the kernel; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[key]
+        if e.get("source_sha") != kernel_source_hash(kernel_file):
+            return None
+        return e["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class Timer:
+    """Per-step CUDA-event timing on a stream, with an L2 flush between steps (not timed)."""
+
+    def __init__(self, stream, flush_buf):
+        self.stream = stream
+        self.flush_buf = flush_buf
+        self.ms = []
+
+    def flush(self):
+        with torch.cuda.stream(self.stream):
+            self.flush_buf.add_(1)
+
+    def run(self, fn, steps, warmup, sections=None):
+        for _ in range(warmup):
+            self.flush()
+            fn(None)
+        torch.cuda.synchronize()
+        self.ms = []
+        sec = {} if sections is None else sections
+        for _ in range(steps):
+            self.flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            marks = []
+            e0.record(self.stream)
+            fn(marks)
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            self.ms.append(e0.elapsed_time(e1))
+            for name, a, b in marks:
+                sec.setdefault(name, []).append(a.elapsed_time(b))
+        return self.ms, sec
+
+
+def mark(marks, name, stream, fn):
+    """Run fn, recording events around it on `stream` when marks is a list."""
+    if marks is None:
+        return fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    r = fn()
+    b.record(stream)
+    marks.append((name, a, b))
+    return r
+
+
+# ---- workloads ----------------------------------------------------------------------------------
+
+def decode_workload(pkv, dev, seed_off=0):
+    cfg = dict(gen.DECODE_QWEN3)
+    cfg["seed"] += seed_off
+    b = gen.decode_batch(**cfg, device=dev)
+    R = b.R
+    meta = dict(cu_q=b.cu_q.to(dev), seq_lens=b.seq_lens.to(dev), block_tables=b.block_tables.to(dev),
+                slot_mapping=b.slot_mapping.to(dev))
+    maxs = max(b.seq_lens_list)
+    kv_bytes = sum(b.seq_lens_list) * b.Hkv * b.D * 2 * 2
+    other = (b.q.numel() * 2 * 2 + R * b.Hq * 4 + sum((s + 15) // 16 for s in b.seq_lens_list) * 4)
+    ws_n = pkv.paged_decode_workspace_size(R, b.Hq, b.Hkv, b.D, maxs)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(b.q)
+    lse = torch.empty((R, b.Hq), dtype=torch.float32, device=dev)
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    bounds = torch.empty(4, dtype=torch.int32, device=dev)
+    cu_r = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    return dict(b=b, meta=meta, maxs=maxs, kv_bytes=kv_bytes, alg_bytes=kv_bytes + other, ws=ws, out=out,
+                lse=lse, perm=perm, bounds=bounds, cu_r=cu_r)
+
+
+def decode_step(pkv, w, stream, marks=None, q=None, meta=None, k_new=None, v_new=None, out=None, lse=None):
+    b = w["b"]
+    meta = meta or w["meta"]
+    q = b.q if q is None else q
+    k_new = b.k_new if k_new is None else k_new
+    v_new = b.v_new if v_new is None else v_new
+    out = w["out"] if out is None else out
+    lse = w["lse"] if lse is None else lse
+    R = b.R
+    pkv.batch_classify_reorder(meta["cu_q"], meta["seq_lens"], perm=w["perm"], bounds=w["bounds"],
+                               cu_q_reordered=w["cu_r"], stream=stream)
+    pkv.kv_cache_write(k_new, v_new, meta["slot_mapping"], b.k_cache, b.v_cache, stream=stream)
+    reqs = pkv.Reqs(max_reqs=R, batch_reqs=R, order=w["perm"], bounds=w["bounds"], cls=pkv.CLASS_DECODE)
+    mark(marks, "decode", stream, lambda: pkv.paged_decode_attn(
+        q, b.k_cache, b.v_cache, meta["block_tables"], meta["seq_lens"], w["maxs"], cu_q=meta["cu_q"],
+        reqs=reqs, scale=1.0 / math.sqrt(b.D), out=out, lse=lse, workspace=w["ws"], stream=stream))
+
+
+def bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=0):
+    w = decode_workload(pkv, dev, seed_off)
+    n0 = pkv.launch_count()
+    ms, sec = timer.run(lambda m: decode_step(pkv, w, stream, m), steps, warmup)
+    launches = (pkv.launch_count() - n0) // (steps + warmup)
+    return w, ms, sec, launches
+
+
+def bench_decode_e2e(pkv, w, dev, stream, steps, warmup):
+    """The same step through the public API with host buffers: the step's inputs (q, new K/V,
+    metadata) are copied from pinned host memory and out/lse read back, inside the timed region.
+    The KV cache stays resident (it is the state of the server)."""
+    b = w["b"]
+    hq = b.q.cpu().pin_memory()
+    hk = b.k_new.cpu().pin_memory()
+    hv = b.v_new.cpu().pin_memory()
+    hmeta = {k: v.cpu().pin_memory() for k, v in w["meta"].items()}
+    hout = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(w["lse"].shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
+    dmeta = {k: torch.empty_like(v) for k, v in w["meta"].items()}
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + sum(v.numel() * v.element_size() for v in hmeta.values())
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    def step():
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            for k in dmeta:
+                dmeta[k].copy_(hmeta[k], non_blocking=True)
+        decode_step(pkv, w, stream, None, q=dq, meta=dmeta, k_new=dk, v_new=dv)
+        with torch.cuda.stream(stream):
+            hout.copy_(w["out"], non_blocking=True)
+            hlse.copy_(w["lse"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return ms, h2d, d2h
+
+
+def mixed_workload(dev):
+    b = gen.mixed_batch(**gen.MIXED_LLAMA70B, device=dev)
+    return b
+
+
+def bench_mixed(pkv, dev, stream, timer, steps, warmup):
+    b = mixed_workload(dev)
+    g = b
+    R, T = b.R, b.T
+    meta = dict(cu_q=b.cu_q.to(dev), seq_lens=b.seq_lens.to(dev), block_tables=b.block_tables.to(dev),
+                slot_mapping=b.slot_mapping.to(dev))
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    bounds = torch.empty(4, dtype=torch.int32, device=dev)
+    cu_r = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(b.q)
+    lse = torch.empty((T, b.Hq), dtype=torch.float32, device=dev)
+    kinds = b.kinds
+    # host-side bounds the scheduler knows: class sizes and maxima per class
+    n_dec = sum(k == gen.DECODE for k in kinds)
+    n_ext = sum(k == gen.EXTEND for k in kinds)
+    n_pre = sum(k == gen.PREFILL for k in kinds)
+    max_dec = max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.DECODE)
+    max_ext_q = max(q for k, q in zip(kinds, b.q_lens) if k == gen.EXTEND)
+    max_ext_s = max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.EXTEND)
+    max_pre = max(q for k, q in zip(kinds, b.q_lens) if k == gen.PREFILL)
+    ws_n = pkv.paged_decode_workspace_size(n_dec, b.Hq, b.Hkv, b.D, max_dec)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(b.D)
+
+    def step(marks):
+        mark(marks, "reorder", stream, lambda: pkv.batch_classify_reorder(
+            meta["cu_q"], meta["seq_lens"], perm=perm, bounds=bounds, cu_q_reordered=cu_r, stream=stream))
+        mark(marks, "write", stream, lambda: pkv.kv_cache_write(
+            g.k_new, g.v_new, meta["slot_mapping"], g.k_cache, g.v_cache, stream=stream))
+        mark(marks, "decode", stream, lambda: pkv.paged_decode_attn(
+            g.q, g.k_cache, g.v_cache, meta["block_tables"], meta["seq_lens"], max_dec, cu_q=meta["cu_q"],
+            reqs=pkv.Reqs(n_dec, R, perm, bounds, pkv.CLASS_DECODE), scale=scale, out=out, lse=lse,
+            workspace=ws, stream=stream))
+        mark(marks, "extend", stream, lambda: pkv.extend_attn(
+            g.q, g.k_new, g.v_new, meta["cu_q"], meta["seq_lens"], g.k_cache, g.v_cache,
+            meta["block_tables"], max_ext_q, max_ext_s, reqs=pkv.Reqs(n_ext, R, perm, bounds, pkv.CLASS_EXTEND),
+            chunk_budget_tokens=32768, scale=scale, out=out, lse=lse, stream=stream))
+        mark(marks, "prefill", stream, lambda: pkv.varlen_prefill_attn(
+            g.q, g.k_new, g.v_new, meta["cu_q"], max_pre, reqs=pkv.Reqs(n_pre, R, perm, bounds, pkv.CLASS_PREFILL),
+            scale=scale, out=out, lse=lse, stream=stream))
+
+    n0 = pkv.launch_count()
+    ms, sec = timer.run(step, steps, warmup)
+    launches = (pkv.launch_count() - n0) // (steps + warmup)
+    dec_bytes = sum(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.DECODE) * b.Hkv * b.D * 4
+    ext_flops = sum(4 * b.Hq * b.D * (q * (s - q) + q * (q + 1) // 2)
+                    for k, q, s in zip(kinds, b.q_lens, b.seq_lens_list) if k == gen.EXTEND)
+    pre_flops = sum(4 * b.Hq * b.D * q * (q + 1) // 2 for k, q in zip(kinds, b.q_lens) if k == gen.PREFILL)
+    return dict(b=b, ms=ms, sec=sec, launches=launches, tokens=T, dec_bytes=dec_bytes,
+                ext_flops=ext_flops, pre_flops=pre_flops)
+
+
+def bench_attention_only(pkv, dev, stream, timer, steps, warmup, kind):
+    """Prefill 4 x 8192 or the long-context extend (2 x (100k cached + 2048 new))."""
+    if kind == "prefill":
+        b = gen.prefill_batch([8192] * 4, Hq=64, Hkv=8, D=128, seed=5, device=dev)
+        flops = sum(4 * b.Hq * b.D * q * (q + 1) // 2 for q in b.q_lens)
+    else:
+        b = gen.extend_batch(**gen.LONG_EXTEND, device=dev)
+        flops = sum(4 * b.Hq * b.D * (q * (s - q) + q * (q + 1) // 2) for q, s in zip(b.q_lens, b.seq_lens_list))
+    out = torch.empty_like(b.q)
+    lse = torch.empty((b.T, b.Hq), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(b.D)
+    meta = dict(cu_q=b.cu_q.to(dev), seq_lens=b.seq_lens.to(dev), block_tables=b.block_tables.to(dev))
+
+    def step(marks):
+        if kind == "prefill":
+            mark(marks, kind, stream, lambda: pkv.varlen_prefill_attn(
+                b.q, b.k_new, b.v_new, meta["cu_q"], max(b.q_lens), scale=scale, out=out, lse=lse, stream=stream))
+        else:
+            mark(marks, kind, stream, lambda: pkv.extend_attn(
+                b.q, b.k_new, b.v_new, meta["cu_q"], meta["seq_lens"], b.k_cache, b.v_cache,
+                meta["block_tables"], max(b.q_lens), max(b.seq_lens_list), chunk_budget_tokens=32768,
+                scale=scale, out=out, lse=lse, stream=stream))
+
+    ms, sec = timer.run(step, steps, warmup)
+    return dict(ms=ms, sec=sec, flops=flops)
+
+
+def bench_write_pack(pkv, dev, stream, timer, steps, warmup):
+    layers = gen.write_pack_layers(**gen.WRITE_PACK_LLAMA70B, device=dev)
+    L0 = layers[0]
+    nblk = L0.block_ids.numel()
+    dst = torch.empty((2, nblk) + tuple(L0.k_cache.shape[1:]), dtype=torch.bfloat16, device=dev)
+    row_bytes = L0.key.numel() * 2
+    write_bytes = len(layers) * (2 * row_bytes * 2 + L0.slot_mapping.numel() * 8)   # read + write, K and V
+    pack_bytes = len(layers) * (2 * dst.numel() * 2 // 1 + nblk * 4)   # read + write
+
+    def step(marks):
+        def w():
+            for L in layers:
+                pkv.kv_cache_write(L.key, L.value, L.slot_mapping, L.k_cache, L.v_cache, stream=stream)
+
+        def p():
+            for L in layers:
+                pkv.kv_block_pack(L.k_cache, L.v_cache, L.block_ids, dst=dst, stream=stream)
+        mark(marks, "write", stream, w)
+        mark(marks, "pack", stream, p)
+
+    ms, sec = timer.run(step, steps, warmup)
+    del layers
+    return dict(ms=ms, sec=sec, write_bytes=write_bytes, pack_bytes=pack_bytes)
+
+
+# ---- CPU oracle ---------------------------------------------------------------------------------
+
+def oracle_decode_rate(b, budget_s=15.0, host=None):
+    """KV GB/s of the fp64 oracle on the decode workload: whole requests in chunks until the
+    time budget is spent (at least one chunk)."""
+    import oracle
+    threads = oracle.default_threads()
+    if host is None:
+        host = dict(q=gen.bf16_bits(b.q), kc=gen.bf16_bits(b.k_cache), vc=gen.bf16_bits(b.v_cache),
+                    bt=b.block_tables.cpu().numpy(), sl=b.seq_lens.cpu().numpy(), cu=b.cu_q.cpu().numpy())
+    R = b.R
+    chunk = max(1, threads)
+    done, t_total, kv = 0, 0.0, 0
+    out = np.empty((b.T, b.Hq, b.D))
+    lse = np.empty((b.T, b.Hq))
+    while done < R and (t_total < budget_s or done == 0):
+        ids = np.arange(done, min(R, done + chunk), dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_decode(host["q"], host["kc"], host["vc"], host["bt"], host["sl"], 1.0 / math.sqrt(b.D),
+                            cu_q=host["cu"], req_ids=ids, nthreads=threads, out=out, lse=lse)
+        t_total += time.perf_counter() - t0
+        kv += int(host["sl"][ids].sum()) * b.Hkv * b.D * 4
+        done += len(ids)
+    return dict(value=kv / t_total / 1e9, unit="GB/s", cores=threads, kind="oracle",
+                sample=f"{done} of {R} requests of the decode workload, whole requests, fp64 C++ oracle, "
+                       f"{t_total:.1f} s")
+
+
+# ---- main ---------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--oracle-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    steps, warmup = args.steps, max(3, args.warmup)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        b = gen.decode_batch(**gen.DECODE_QWEN3, device="cpu")
+        times, vals = [], []
+        host = dict(q=gen.bf16_bits(b.q), kc=gen.bf16_bits(b.k_cache), vc=gen.bf16_bits(b.v_cache),
+                    bt=b.block_tables.numpy(), sl=b.seq_lens.numpy(), cu=b.cu_q.numpy())
+        budget = max(2.0, 120.0 / max(1, steps + warmup))
+        for i in range(warmup + steps):
+            r = oracle_decode_rate(b, budget_s=budget, host=host)
+            if i >= warmup:
+                vals.append(r["value"])
+        v = statistics.median(vals)
+        line = {"impl": "reference", "metric": "paged decode attn KV GB/s (frac of HBM peak); mixed-batch attn tokens/s",
+                "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": "decode-only Qwen3-235B-like: B=256, ctx U[2000,3000], "
+                                                            "Hq 64 / Hkv 4, D 128, bs 16"},
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import paged_kv_attention_reshape_gb300 as pkv
+    pkv.load()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    timer = Timer(stream, flush_buf)
+    peaks = load_peaks()
+
+    clocks = Clocks(local)
+    with clocks:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        w, ms, sec, launches = bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=rank)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    step_ms = sum(ms) / len(ms)
+    if ws > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = ws * w["kv_bytes"] / (step_ms * 1e-3) / 1e9
+    dec_ms = sum(sec["decode"]) / len(sec["decode"])
+    achieved = w["alg_bytes"] / (dec_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("decode.cu", "paged_decode_qwen3")
+    e2e_ms, h2d, d2h = bench_decode_e2e(pkv, w, dev, stream, steps, warmup)
+    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    line = {
+        "metric": "paged decode attn KV GB/s (frac of HBM peak); mixed-batch attn tokens/s",
+        "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode-only Qwen3-235B-like attention layer: 256 seqs, ctx U[2000,3000], "
+                               "Hq 64 / Hkv 4, head_dim 128, block 16, pool 1.2x, shuffled blocks; "
+                               "step = reorder + kv_cache_write + paged_decode_attn",
+                   "kv_bytes_per_step": w["kv_bytes"], "l2": "512 MiB buffer written between timed steps; "
+                   "KV read per step (1.3 GB) is also larger than L2", "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": "paged_decode_kernel (+ split merge)", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                     "traffic": traffic, "algorithmic_bytes_per_launch": w["alg_bytes"],
+                     "peak_source": peaks["source"] + " (hbm copy, burst)", "launch_ms": dec_ms},
+        "frac_of_nominal_8TBs": w["kv_bytes"] / (dec_ms * 1e-3) / 8e12,
+        "e2e": {"value": ws * w["kv_bytes"] / (e2e_step * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
+        "gpu_launches": launches * steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed": t_wall,
+    }
+    if not args.no_extras and rank == 0:
+        extras = {}
+        try:
+            m = bench_mixed(pkv, dev, stream, timer, steps, warmup)
+            mms = sum(m["ms"]) / len(m["ms"])
+            per = {k: sum(v) / len(v) for k, v in m["sec"].items()}
+            extras["mixed_batch"] = {
+                "workload": "Llama-3.1-70B-like layer (Hq 64 / Hkv 8, D 128): 192 decode ctx U[1000,8000], "
+                            "8 extend 512 new over U[4000,32000] cached, 4 prefill U[2000,8000], shuffled",
+                "tokens_per_s": m["tokens"] / (mms * 1e-3), "ms_per_step": mms, "tokens": m["tokens"],
+                "per_call_ms": per, "gpu_launches_per_step": m["launches"],
+                "decode_kv_gbs": m["dec_bytes"] / (per["decode"] * 1e-3) / 1e9,
+                "extend_tflops": m["ext_flops"] / (per["extend"] * 1e-3) / 1e12,
+                "prefill_tflops": m["pre_flops"] / (per["prefill"] * 1e-3) / 1e12,
+                "bound_ms": (m["dec_bytes"] / (peaks["hbm"] * 1e9) + (m["ext_flops"] + m["pre_flops"]) /
+                             (peaks["bf16_sust"] * 1e12)) * 1e3,
+            }
+            extras["mixed_batch"]["frac_of_bound"] = extras["mixed_batch"]["bound_ms"] / mms
+            del m
+        except Exception as e:  # report, keep the headline
+            extras["mixed_batch"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        for kind in ("prefill", "extend_long"):
+            try:
+                r = bench_attention_only(pkv, dev, stream, timer, max(3, steps // 2), warmup,
+                                         "prefill" if kind == "prefill" else "extend")
+                k = "prefill" if kind == "prefill" else "extend"
+                t = sum(r["sec"][k]) / len(r["sec"][k])
+                tf = r["flops"] / (t * 1e-3) / 1e12
+                extras[kind] = {"workload": "4 x 8192 prompts, Hq 64 / Hkv 8, D 128" if kind == "prefill"
+                                else "2 x (100000 cached + 2048 new), Hq 64 / Hkv 8, D 128, budget 32768",
+                                "tflops": tf, "ms": t, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                "peak_tflops": peaks["bf16"], "peak_source": peaks["source"] + " (bf16 burst)"}
+            except Exception as e:
+                extras[kind] = {"error": repr(e)}
+            torch.cuda.empty_cache()
+        try:
+            r = bench_write_pack(pkv, dev, stream, timer, max(3, steps // 2), warmup)
+            tw = sum(r["sec"]["write"]) / len(r["sec"]["write"])
+            tp = sum(r["sec"]["pack"]) / len(r["sec"]["pack"])
+            extras["write_pack"] = {"workload": "80 layers x 10000 tokens, Hkv 8, D 128 (320 KiB/token)",
+                                    "write_gbs": r["write_bytes"] / (tw * 1e-3) / 1e9,
+                                    "pack_gbs": r["pack_bytes"] / (tp * 1e-3) / 1e9,
+                                    "write_ms_80_layers": tw, "pack_ms_80_layers": tp,
+                                    "write_frac": r["write_bytes"] / (tw * 1e-3) / 1e9 / peaks["hbm"],
+                                    "pack_frac": r["pack_bytes"] / (tp * 1e-3) / 1e9 / peaks["hbm"]}
+        except Exception as e:
+            extras["write_pack"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        line["extras"] = extras
+    if rank == 0:
+        line["cpu_baseline"] = oracle_decode_rate(w["b"], budget_s=args.oracle_seconds)
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

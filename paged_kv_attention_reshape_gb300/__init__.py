@@ -1,0 +1,10 @@
+"""Paged-KV attention for mixed decode / extend / prefill batches on NVIDIA GB300 (sm_103a).
+
+The computation lives in libpkv.so (hand-written CUDA behind the C ABI of include/pkv.h);
+this package only builds, loads and calls it.
+"""
+from .binding import (  # noqa: F401
+    CLASS_DECODE, CLASS_EXTEND, CLASS_PREFILL, PkvError, Reqs, batch_classify_reorder,
+    device_errors, extend_attn, kv_block_pack, kv_cache_write, launch_count, make_cache,
+    paged_decode_attn, paged_decode_workspace_size, varlen_prefill_attn)
+from ._lib import lib_path, load  # noqa: F401

@@ -1,0 +1,402 @@
+// api.cu — the C ABI (include/pkv.h): host-side argument checks, TMA descriptor encoding,
+// launch-shape heuristics and the per-device error word. Every compute step runs in the
+// kernels of the other files; nothing here touches tensor data.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+
+namespace pkv {
+
+// The per-device error word: a file-scope device variable (each device that loads the
+// library has its own copy). Kernels receive its address (cudaGetSymbolAddress).
+__device__ unsigned int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local int64_t t_launches = 0;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+unsigned int* error_word() {
+  static std::mutex mu;
+  static unsigned int* addr[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (addr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[d] = static_cast<unsigned int*>(p);
+  }
+  return addr[d];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// TMA map over a token-major tensor [rows, heads, D] (bf16): dims (64, heads*D/64, rows),
+// box 64 x 1 x box_rows, 128-byte swizzle. One box = one 64-wide half of one head's rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads) * (D / 64), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(heads) * D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TMA map over one paged cache tensor: dims (64, Hkv*D/64, block_size, num_blocks), box
+// 64 x 1 x block_size x 1 (one 64-wide half of one head of one block), 128-byte swizzle.
+bool encode_cache(CUtensorMap* m, const void* base, const pkv_cache& c) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int D = c.head_dim;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(c.num_kv_heads) * (D / 64),
+                        static_cast<cuuint64_t>(c.block_size), static_cast<cuuint64_t>(c.num_blocks)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(c.num_kv_heads) * D * 2,
+                           static_cast<cuuint64_t>(c.stride_block) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(c.block_size), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool group_ok(int Hq, int Hkv) {
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+}
+
+// Common checks of a cache descriptor. attention: the stricter shape set of the attention calls.
+pkv_status check_cache(const pkv_cache& c, bool attention) {
+  if (c.k == nullptr || c.v == nullptr || c.num_blocks <= 0 || c.block_size <= 0 ||
+      c.num_kv_heads <= 0 || c.head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(c.k) || !aligned16(c.v)) return PKV_ERR_INVALID_ARG;
+  const int64_t blk_elems = static_cast<int64_t>(c.block_size) * c.num_kv_heads * c.head_dim;
+  if (c.stride_block < blk_elems || (c.stride_block * 2) % 16 != 0) return PKV_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(c.num_kv_heads) * c.head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (attention) {
+    if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (c.block_size != 16) return PKV_ERR_UNSUPPORTED;
+  }
+  return PKV_OK;
+}
+
+pkv_status check_reqs(const pkv_reqs& r) {
+  if (r.max_reqs < 0 || r.batch_reqs < 0) return PKV_ERR_INVALID_ARG;
+  if (r.bounds != nullptr && (r.cls < 0 || r.cls > 2)) return PKV_ERR_INVALID_ARG;
+  if (r.order == nullptr && r.bounds == nullptr && r.max_reqs > r.batch_reqs) return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Split-KV shape for decode: enough CTAs to fill the GPU a few times over, each split at
+// least 256 tokens, split length a multiple of the block size.
+void decode_split(int max_reqs, int Hkv, int max_seq_len, int sms, int* split_tokens,
+                  int* max_splits) {
+  const int64_t units = static_cast<int64_t>(max_reqs) * Hkv;
+  const int64_t target = static_cast<int64_t>(sms) * 8;
+  int splits = units > 0 ? static_cast<int>((target + units - 1) / units) : 1;
+  const int cap = max(1, (max_seq_len + 255) / 256);
+  splits = max(1, min(splits, cap));
+  int st = (max_seq_len + splits - 1) / splits;
+  st = max(16, (st + 15) / 16 * 16);
+  *split_tokens = st;
+  *max_splits = max(1, (max_seq_len + st - 1) / st);
+}
+
+}  // namespace
+
+int num_sms() {
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[d] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 148;
+    cache[d] = v;
+  }
+  return cache[d];
+}
+
+cudaError_t set_smem_attr_once(const void* func, int bytes, int slot) {
+  static std::mutex mu;
+  static bool done[kAttrCount][kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(mu);
+  if (done[slot][d]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[slot][d] = true;
+  return e;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE: return "device-side index error";
+  }
+  return "unknown status";
+}
+
+int64_t pkv_launch_count(int32_t reset) {
+  const int64_t v = t_launches;
+  if (reset) t_launches = 0;
+  return v;
+}
+
+pkv_status pkv_device_errors(uint32_t* flags, int32_t clear, pkv_stream_t stream) {
+  if (flags == nullptr) return PKV_ERR_INVALID_ARG;
+  unsigned int* w = error_word();
+  if (w == nullptr) return PKV_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, w, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (clear && cudaMemsetAsync(w, 0, sizeof v, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  *flags = v;
+  return v ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+pkv_status pkv_kv_cache_write(const void* key, const void* value, const int64_t* slot_mapping,
+                              int64_t num_tokens, pkv_cache cache, pkv_stream_t stream) {
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if (num_tokens == 0) return PKV_OK;
+  if (key == nullptr || value == nullptr || slot_mapping == nullptr) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value)) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > (int64_t(1) << 40)) return PKV_ERR_INVALID_ARG;
+  st = cuda_status(launch_kv_cache_write(key, value, slot_mapping, num_tokens, cache, error_word(),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+  t_launches += 1;
+  return st;
+}
+
+pkv_status pkv_kv_block_pack(pkv_cache cache, const int32_t* block_ids, int32_t num_ids, void* dst,
+                             pkv_stream_t stream) {
+  if (num_ids < 0) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if (num_ids == 0) return PKV_OK;
+  if (block_ids == nullptr || dst == nullptr || !aligned16(dst)) return PKV_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * 2) % 16 != 0)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_ids > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
+  st = cuda_status(launch_kv_block_pack(cache, block_ids, num_ids, dst, error_word(),
+                                        reinterpret_cast<cudaStream_t>(stream)));
+  t_launches += 1;
+  return st;
+}
+
+pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens,
+                                      int32_t num_reqs, int32_t decode_threshold, int32_t* perm,
+                                      int32_t* bounds, int32_t* cu_q_reordered, int32_t* token_map,
+                                      int64_t num_tokens, pkv_stream_t stream) {
+  if (num_reqs < 0 || num_reqs > 65536 || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (bounds == nullptr) return PKV_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (cu_q == nullptr || seq_lens == nullptr || perm == nullptr))
+    return PKV_ERR_INVALID_ARG;
+  if (token_map != nullptr && cu_q_reordered == nullptr) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  int launches = 0;
+  pkv_status st = cuda_status(launch_batch_classify_reorder(
+      cu_q, seq_lens, num_reqs, decode_threshold, perm, bounds, cu_q_reordered, token_map,
+      num_tokens, reinterpret_cast<cudaStream_t>(stream), &launches));
+  t_launches += launches;
+  return st;
+}
+
+size_t pkv_paged_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t max_seq_len) {
+  if (max_reqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0) return 0;
+  int st, ms;
+  decode_split(max_reqs, num_kv_heads, max_seq_len, num_sms(), &st, &ms);
+  if (ms <= 1) return 0;
+  const size_t n = static_cast<size_t>(max_reqs) * num_q_heads * ms;
+  return n * head_dim * sizeof(float) + n * sizeof(float);
+}
+
+pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
+                                 int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_q,
+                                 pkv_reqs reqs, int32_t num_q_heads, int32_t max_seq_len,
+                                 float scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, pkv_stream_t stream) {
+  pkv_status st = check_cache(cache, true);
+  if (st != PKV_OK) return st;
+  if ((st = check_reqs(reqs)) != PKV_OK) return st;
+  if (!group_ok(num_q_heads, cache.num_kv_heads)) return PKV_ERR_UNSUPPORTED;
+  if (max_blocks <= 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs == 0) return PKV_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs > 65535) return PKV_ERR_UNSUPPORTED;
+  DecodeParams p{};
+  p.err = error_word();
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.block_tables = block_tables;
+  p.max_blocks = max_blocks;
+  p.seq_lens = seq_lens;
+  p.cu_q = cu_q;
+  p.order = reqs.order;
+  p.bounds = reqs.bounds;
+  p.cls = reqs.cls;
+  p.max_reqs = reqs.max_reqs;
+  p.batch_reqs = reqs.batch_reqs;
+  p.Hq = num_q_heads;
+  p.Hkv = cache.num_kv_heads;
+  p.G = num_q_heads / cache.num_kv_heads;
+  p.num_blocks = cache.num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  decode_split(reqs.max_reqs, cache.num_kv_heads, max_seq_len, num_sms(), &p.split_tokens,
+               &p.max_splits);
+  if (p.max_splits > 1) {
+    const size_t need = pkv_paged_decode_workspace_size(reqs.max_reqs, num_q_heads,
+                                                        cache.num_kv_heads, cache.head_dim,
+                                                        max_seq_len);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return PKV_ERR_WORKSPACE;
+    const size_t n = static_cast<size_t>(reqs.max_reqs) * num_q_heads * p.max_splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = p.ws_o + n * cache.head_dim;
+  }
+  if (p.max_splits > 65535) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
+  int launches = 0;
+  st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim,
+                                       reinterpret_cast<cudaStream_t>(stream), &launches));
+  t_launches += launches;
+  return st;
+}
+
+size_t pkv_extend_workspace_size(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
+
+// Extend (cache != NULL) and prefill (cache == NULL) share the checks and the kernel.
+static pkv_status run_attention(const void* q, const void* k, const void* v, int64_t num_tokens,
+                                const int32_t* cu_q, const int32_t* seq_lens,
+                                const pkv_cache* cache, const int32_t* block_tables,
+                                int32_t max_blocks, pkv_reqs reqs, int32_t Hq, int32_t Hkv,
+                                int32_t D, int32_t max_q_len, int32_t max_seq_len, float scale,
+                                void* out, float* lse, pkv_stream_t stream) {
+  pkv_status st = check_reqs(reqs);
+  if (st != PKV_OK) return st;
+  if (cache != nullptr && (st = check_cache(*cache, true)) != PKV_OK) return st;
+  if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
+  if (!group_ok(Hq, Hkv)) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
+  if (num_tokens > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (q == nullptr || k == nullptr || v == nullptr || cu_q == nullptr || out == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (cache != nullptr && (seq_lens == nullptr || block_tables == nullptr || max_blocks <= 0))
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  AttnParams p{};
+  p.err = error_word();
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.cu_q = cu_q;
+  p.seq_lens = cache ? seq_lens : nullptr;
+  p.block_tables = cache ? block_tables : nullptr;
+  p.max_blocks = cache ? max_blocks : 0;
+  p.order = reqs.order;
+  p.bounds = reqs.bounds;
+  p.cls = reqs.cls;
+  p.max_reqs = reqs.max_reqs;
+  p.batch_reqs = reqs.batch_reqs;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.num_blocks = cache ? cache->num_blocks : 0;
+  p.num_tokens = num_tokens;
+  p.max_q_len = max_q_len;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  CUtensorMap tq, tk, tv, tck, tcv;
+  std::memset(&tck, 0, sizeof tck);
+  std::memset(&tcv, 0, sizeof tcv);
+  if (!encode_rows(&tq, q, num_tokens, Hq, D, 64) || !encode_rows(&tk, k, num_tokens, Hkv, D, 64) ||
+      !encode_rows(&tv, v, num_tokens, Hkv, D, 64))
+    return PKV_ERR_CUDA;
+  if (cache != nullptr &&
+      (!encode_cache(&tck, cache->k, *cache) || !encode_cache(&tcv, cache->v, *cache)))
+    return PKV_ERR_CUDA;
+  int launches = 0;
+  st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D,
+                                    reinterpret_cast<cudaStream_t>(stream), &launches));
+  t_launches += launches;
+  return st;
+}
+
+pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, int64_t num_tokens,
+                           const int32_t* cu_q, const int32_t* seq_lens, pkv_cache cache,
+                           const int32_t* block_tables, int32_t max_blocks, pkv_reqs reqs,
+                           int32_t num_q_heads, int32_t max_q_len, int32_t max_seq_len,
+                           int32_t chunk_budget_tokens, float scale, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (chunk_budget_tokens < 0) return PKV_ERR_INVALID_ARG;
+  return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &cache, block_tables,
+                       max_blocks, reqs, num_q_heads, cache.num_kv_heads, cache.head_dim,
+                       max_q_len, max_seq_len, scale, out, lse, stream);
+}
+
+pkv_status pkv_varlen_prefill_attn(const void* q, const void* k, const void* v, int64_t num_tokens,
+                                   const int32_t* cu_seqlens, pkv_reqs reqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t max_seqlen,
+                                   float scale, void* out, float* lse, pkv_stream_t stream) {
+  return run_attention(q, k, v, num_tokens, cu_seqlens, nullptr, nullptr, nullptr, 0, reqs,
+                       num_q_heads, num_kv_heads, head_dim, max_seqlen, max_seqlen, scale, out,
+                       lse, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// launch.h — parameter blocks and launchers shared between the C-ABI layer (api.cu) and the
+// kernel files. Host and device code see the same plain structs.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+struct DecodeParams {
+  unsigned int* err;  // device error word
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  const int32_t* order;
+  const int32_t* bounds;
+  int32_t cls;
+  int32_t max_reqs;
+  int32_t batch_reqs;
+  int32_t Hq, Hkv, G;
+  int64_t num_blocks;
+  int32_t max_seq_len;
+  float scale_log2;      // softmax scale * log2(e)
+  int32_t split_tokens;  // tokens per split (multiple of the block size)
+  int32_t max_splits;
+  float* ws_o;           // [max_reqs, Hq, max_splits, D] normalised partial outputs
+  float* ws_lse;         // [max_reqs, Hq, max_splits] natural-log partial LSE
+};
+
+// Extend and prefill share one kernel; prefill is the case without cached context.
+struct AttnParams {
+  unsigned int* err;  // device error word
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* cu_q;
+  const int32_t* seq_lens;      // NULL for prefill (no cached context)
+  const int32_t* block_tables;  // NULL for prefill
+  int32_t max_blocks;
+  const int32_t* order;
+  const int32_t* bounds;
+  int32_t cls;
+  int32_t max_reqs;
+  int32_t batch_reqs;
+  int32_t Hq, Hkv, G;
+  int64_t num_blocks;
+  int64_t num_tokens;           // rows of q / k_new / v_new
+  int32_t max_q_len;
+  int32_t max_seq_len;
+  float scale_log2;
+};
+
+// Indices into the per-device "dynamic shared memory attribute set" table.
+enum AttrSlot {
+  kAttrDecode64 = 0,
+  kAttrDecode128,
+  kAttrAttn64,
+  kAttrAttn128,
+  kAttrCount
+};
+
+// Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (kernel slot, device).
+cudaError_t set_smem_attr_once(const void* func, int bytes, int slot);
+
+int num_sms();  // of the current device (cached per device)
+
+cudaError_t launch_kv_cache_write(const void* key, const void* value, const int64_t* slot_mapping,
+                                  int64_t num_tokens, const pkv_cache& c, unsigned int* err,
+                                  cudaStream_t stream);
+cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, int32_t num_ids,
+                                 void* dst, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens, int32_t R,
+                                          int32_t threshold, int32_t* perm, int32_t* bounds,
+                                          int32_t* cu_q_reordered, int32_t* token_map,
+                                          int64_t num_tokens, cudaStream_t stream, int* launches);
+cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                int D, cudaStream_t stream, int* launches);
+int decode_smem_bytes(int D);
+// tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
+// (ignored for prefill).
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                             const CUtensorMap& tm_v, const CUtensorMap& tm_ck,
+                             const CUtensorMap& tm_cv, int D, cudaStream_t stream, int* launches);
+
+}  // namespace pkv

@@ -1,0 +1,285 @@
+"""GPU parity of every call against the oracle at sizes the oracle finishes in seconds, covering
+several tiles, ragged tails and the degenerate cases. Indexing calls bit-exact; attention within
+the stated tolerances (tests/helpers.py)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pkv_workloads import gen
+
+from helpers import bits, compare_attention, default_scale, oracle_decode, oracle_extend, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_attention_reshape_gb300 as m
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+DEV = "cuda"
+
+
+def _errors(pkv):
+    return pkv.device_errors(clear=True)
+
+
+# ---- kv_cache_write --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Hkv,D", [(2, 64), (8, 128), (1, 8)])
+def test_kv_cache_write_bit_exact(pkv, Hkv, D):
+    b = gen.mixed_batch(5, (3, 70), 3, 20, (1, 50), 2, (1, 45), Hq=Hkv, Hkv=Hkv, D=D, seed=D + Hkv)
+    slots = b.slot_mapping.clone()
+    slots[::7] = -1
+    g = b.to(DEV)
+    pkv.kv_cache_write(g.k_new, g.v_new, slots.to(DEV), g.k_cache, g.v_cache)
+    kc, vc = bits(b.k_cache).copy(), bits(b.v_cache).copy()
+    assert oracle.kv_cache_write(bits(b.k_new), bits(b.v_new), slots.numpy(), kc, vc) == 0
+    assert np.array_equal(bits(g.k_cache), kc) and np.array_equal(bits(g.v_cache), vc)
+    assert _errors(pkv) == 0
+
+
+def test_kv_cache_write_strided_cache_and_bad_slots(pkv):
+    """K and V in one allocation [nb, 2, bs, H, D]; out-of-range slots are skipped and flagged."""
+    nb, bs, H, D = 12, 16, 2, 64
+    both = gen.randn_bf16((nb, 2, bs, H, D), torch.Generator().manual_seed(3), "cpu")
+    key = gen.randn_bf16((9, H, D), torch.Generator().manual_seed(4), "cpu")
+    val = gen.randn_bf16((9, H, D), torch.Generator().manual_seed(5), "cpu")
+    slots = torch.tensor([0, 5, 17, 191, -1, 40, nb * bs, 1000, 33], dtype=torch.int64)
+    g = both.to(DEV)
+    pkv.kv_cache_write(key.to(DEV), val.to(DEV), slots.to(DEV), g[:, 0], g[:, 1])
+    kc, vc = bits(both[:, 0]).copy(), bits(both[:, 1]).copy()
+    assert oracle.kv_cache_write(bits(key), bits(val), slots.numpy(), kc, vc) == 2
+    gb = bits(g)
+    assert np.array_equal(gb[:, 0], kc) and np.array_equal(gb[:, 1], vc)
+    assert _errors(pkv) & 0x1
+
+
+def test_kv_cache_write_empty(pkv):
+    c = torch.zeros((2, 16, 1, 64), dtype=torch.bfloat16, device=DEV)
+    e = torch.empty((0, 1, 64), dtype=torch.bfloat16, device=DEV)
+    pkv.kv_cache_write(e, e, torch.empty(0, dtype=torch.int64, device=DEV), c, c)
+    assert _errors(pkv) == 0 and c.abs().sum().item() == 0
+
+
+# ---- kv_block_pack ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shuffled", [False, True])
+def test_kv_block_pack_bit_exact(pkv, shuffled):
+    L = gen.write_pack_layers(1, 300, Hkv=8, D=128, seed=8, shuffled_pack=shuffled)[0]
+    gk, gv = L.k_cache.to(DEV), L.v_cache.to(DEV)
+    pkv.kv_cache_write(L.key.to(DEV), L.value.to(DEV), L.slot_mapping.to(DEV), gk, gv)
+    dst = pkv.kv_block_pack(gk, gv, L.block_ids.to(DEV))
+    kc, vc = bits(L.k_cache).copy(), bits(L.v_cache).copy()
+    oracle.kv_cache_write(bits(L.key), bits(L.value), L.slot_mapping.numpy(), kc, vc)
+    exp, bad = oracle.kv_block_pack(kc, vc, L.block_ids.numpy())
+    assert bad == 0 and np.array_equal(bits(dst), exp)
+    assert _errors(pkv) == 0
+
+
+def test_kv_block_pack_duplicates_and_bad_ids(pkv):
+    kc = gen.randn_bf16((6, 16, 2, 64), torch.Generator().manual_seed(1), "cpu")
+    vc = gen.randn_bf16((6, 16, 2, 64), torch.Generator().manual_seed(2), "cpu")
+    ids = torch.tensor([5, 5, 0, 6, -3, 2], dtype=torch.int32)
+    dst0 = torch.zeros((2, 6, 16, 2, 64), dtype=torch.bfloat16)
+    dst = pkv.kv_block_pack(kc.to(DEV), vc.to(DEV), ids.to(DEV), dst=dst0.to(DEV))
+    exp = np.zeros((2, 6, 16, 2, 64), np.uint16)
+    exp, bad = oracle.kv_block_pack(bits(kc), bits(vc), ids.numpy(), dst=exp)
+    assert bad == 2 and np.array_equal(bits(dst), exp)
+    assert _errors(pkv) & 0x2
+
+
+# ---- batch_classify_reorder ------------------------------------------------------------------
+
+def _reorder_case(R, seed, thr=1):
+    rng = np.random.default_rng(seed)
+    kind = rng.integers(0, 3, R)
+    q = np.where(kind == 0, rng.integers(0, 2, R), rng.integers(1, 300, R))
+    cached = np.where(kind == 1, rng.integers(1, 1000, R), 0)
+    cached = np.where(kind == 0, rng.integers(0, 5000, R), cached)
+    seq = q + cached
+    cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+    return cu, seq.astype(np.int32), thr
+
+
+@pytest.mark.parametrize("R,seed,thr", [(0, 0, 1), (1, 1, 1), (204, 2, 1), (1024, 3, 1),
+                                        (1025, 4, 1), (3001, 5, 1), (500, 6, 4), (64, 7, 0)])
+def test_reorder_bit_exact(pkv, R, seed, thr):
+    cu, seq, thr = _reorder_case(R, seed, thr)
+    T = int(cu[-1])
+    perm, bounds, cu_r, tmap = pkv.batch_classify_reorder(
+        torch.from_numpy(cu).to(DEV), torch.from_numpy(seq).to(DEV), decode_threshold=thr,
+        with_token_map=True, num_tokens=T)
+    e_perm, e_bounds, e_cu, e_map = oracle.batch_classify_reorder(cu, seq, thr)
+    assert np.array_equal(perm.cpu().numpy(), e_perm)
+    assert np.array_equal(bounds.cpu().numpy(), e_bounds)
+    assert np.array_equal(cu_r.cpu().numpy(), e_cu)
+    assert np.array_equal(tmap.cpu().numpy(), e_map)
+
+
+def test_reorder_single_class(pkv):
+    cu = np.arange(0, 11, dtype=np.int32)          # ten decode requests
+    seq = np.full(10, 50, np.int32)
+    perm, bounds, _, _ = pkv.batch_classify_reorder(torch.from_numpy(cu).to(DEV), torch.from_numpy(seq).to(DEV))
+    assert perm.tolist() == list(range(10)) and bounds.tolist() == [0, 10, 10, 10]
+
+
+# ---- paged_decode_attn -----------------------------------------------------------------------
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_group_sizes(pkv, G, D):
+    Hkv = 2
+    b = gen.decode_batch(6, 1, 300, Hq=G * Hkv, Hkv=Hkv, D=D, seed=10 * G + D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                                     max(b.seq_lens_list), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode G={G} D={D}")
+    assert _errors(pkv) == 0
+
+
+def test_decode_tiny_config(pkv):
+    """4 sequences, context U[16,200], 8 Q / 2 KV heads, head_dim 64, pool of 64 blocks, seed 0."""
+    b = gen.decode_batch(**gen.TINY_DECODE)
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                                     max(b.seq_lens_list), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what="decode tiny")
+
+
+@pytest.mark.parametrize("ctxs", [[1, 16, 17, 31, 32, 33], [0, 5, 0], [4096, 1, 7000, 15]])
+def test_decode_edge_lengths_and_splits(pkv, ctxs):
+    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=1, D=128, seed=len(ctxs))
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                                     max(ctxs), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode {ctxs}")
+    empty = np.array(ctxs) == 0
+    if empty.any():
+        o = out.float().cpu().numpy()[empty]
+        assert np.all(o == 0) and np.all(np.isneginf(lse.cpu().numpy()[empty]))
+
+
+def test_decode_peaked_softmax(pkv):
+    b = gen.decode_batch(8, 100, 900, Hq=32, Hkv=4, D=128, seed=77, q_scale=4.0)
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                                     max(b.seq_lens_list), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what="decode peaked")
+
+
+def test_decode_nonfinite_past_the_end_is_ignored(pkv):
+    """Cache rows after the last valid token of a block may hold anything (NaN here)."""
+    b = gen.decode_batch(3, 5, 40, Hq=8, Hkv=2, D=64, seed=5)
+    kc = b.k_cache.clone()
+    vc = b.v_cache.clone()
+    bt = b.block_tables.numpy()
+    for r, n in enumerate(b.seq_lens_list):
+        last = bt[r, (n - 1) // 16]
+        kc[last, n % 16 or 16:] = float("nan")
+        vc[last, n % 16 or 16:] = float("nan")
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.paged_decode_attn(g.q, kc.to(DEV), vc.to(DEV), g.block_tables, g.seq_lens,
+                                     max(b.seq_lens_list), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(kc), bits(vc), scale)
+    compare_attention(out, lse, ref, ref_lse, what="decode nan tail")
+
+
+# ---- extend / prefill ------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G,D", [(1, 64), (4, 128), (8, 128), (16, 64), (2, 128)])
+def test_extend_ragged(pkv, G, D):
+    Hkv = 2
+    new = [1, 63, 64, 65, 130, 7]
+    ctx = [0, 1, 15, 16, 100, 300]
+    b = gen.extend_batch(new, ctx, Hq=G * Hkv, Hkv=Hkv, D=D, seed=G * 7 + D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, g.k_cache, g.v_cache,
+                               g.block_tables, max(new), max(b.seq_lens_list), scale=scale)
+    ref, ref_lse = oracle_extend(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"extend G={G} D={D}")
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_ragged(pkv, D):
+    lens = [1, 17, 64, 65, 200, 128, 3]
+    b = gen.prefill_batch(lens, Hq=16, Hkv=4, D=D, seed=D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.varlen_prefill_attn(g.q, g.k_new, g.v_new, g.cu_q, max(lens), scale=scale)
+    ref, ref_lse = oracle_prefill(b, scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"prefill D={D}")
+    assert _errors(pkv) == 0
+
+
+def test_prefill_peaked(pkv):
+    b = gen.prefill_batch([300, 77], Hq=8, Hkv=1, D=128, seed=9, q_scale=4.0)
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.varlen_prefill_attn(g.q, g.k_new, g.v_new, g.cu_q, 300, scale=scale)
+    ref, ref_lse = oracle_prefill(b, scale)
+    compare_attention(out, lse, ref, ref_lse, what="prefill peaked")
+
+
+# ---- the mixed batch through the reorder -----------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_mixed_batch_pipeline(pkv, D):
+    b = gen.mixed_batch(20, (10, 400), 3, 70, (30, 300), 3, (10, 150), Hq=16, Hkv=2, D=D, seed=31 + D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    R, T = b.R, b.T
+    perm, bounds, _, _ = pkv.batch_classify_reorder(g.cu_q, g.seq_lens)
+    pkv.kv_cache_write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    maxs, maxq = max(b.seq_lens_list), max(b.q_lens)
+    mk = lambda c: pkv.Reqs(max_reqs=R, batch_reqs=R, order=perm, bounds=bounds, cls=c)
+    pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, maxs, cu_q=g.cu_q,
+                          reqs=mk(pkv.CLASS_DECODE), scale=scale, out=out, lse=lse)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, g.k_cache, g.v_cache, g.block_tables,
+                    maxq, maxs, reqs=mk(pkv.CLASS_EXTEND), scale=scale, out=out, lse=lse)
+    pkv.varlen_prefill_attn(g.q, g.k_new, g.v_new, g.cu_q, maxq, reqs=mk(pkv.CLASS_PREFILL),
+                            scale=scale, out=out, lse=lse)
+    assert _errors(pkv) == 0
+    kc, vc = bits(b.k_cache).copy(), bits(b.v_cache).copy()
+    oracle.kv_cache_write(bits(b.k_new), bits(b.v_new), b.slot_mapping.numpy(), kc, vc)
+    assert np.array_equal(bits(g.k_cache), kc)
+    e_perm, e_b, _, _ = oracle.batch_classify_reorder(b.cu_q.numpy(), b.seq_lens.numpy())
+    ref = np.full((T, b.Hq, D), np.nan)
+    ref_lse = np.full((T, b.Hq), np.nan)
+    oracle_decode(b, kc, vc, scale, req_ids=e_perm[e_b[0]:e_b[1]], out=ref, lse=ref_lse)
+    oracle_extend(b, kc, vc, scale, req_ids=e_perm[e_b[1]:e_b[2]], out=ref, lse=ref_lse)
+    oracle_prefill(b, scale, req_ids=e_perm[e_b[2]:e_b[3]], out=ref, lse=ref_lse)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, rows=np.ones(T, bool), what=f"mixed D={D}")
+
+
+def test_request_set_cut_to_max_reqs_is_flagged(pkv):
+    b = gen.decode_batch(6, 10, 60, Hq=4, Hkv=1, D=64, seed=2)
+    g = b.to(DEV)
+    bounds = torch.tensor([0, 6, 6, 6], dtype=torch.int32, device=DEV)
+    order = torch.arange(6, dtype=torch.int32, device=DEV)
+    reqs = pkv.Reqs(max_reqs=4, batch_reqs=6, order=order, bounds=bounds, cls=0)
+    out = torch.zeros_like(g.q)
+    pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, 60, cu_q=g.cu_q,
+                          reqs=reqs, out=out)
+    assert _errors(pkv) & 0x4
+    assert out[4:].abs().sum().item() == 0  # requests past the bound are not computed

@@ -176,6 +176,32 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
                                  size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * paged_decode_attn_noalloc — paged_decode_attn for callers that cannot allocate.
+ * The pages have no counterpart to this call; it exists for users of this library who can
+ * pass in input and output buffers but cannot allocate device memory themselves, e.g. an
+ * engine that has given all of its device memory to a fixed KV-cache pool, or a plug-in
+ * whose host program owns every allocation. It computes exactly what paged_decode_attn
+ * computes (same arguments, minus the workspace) and calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ * Its split-KV scratch is one array of PKV_NOALLOC_SCRATCH_BYTES bytes compiled into the
+ * library as a device variable: every GPU that loads the library's device code holds that
+ * memory until the process exits. The first call on a device looks up the array's device
+ * address (with that device current) and caches it; make that first call before any stream
+ * capture. A call whose scratch need, pkv_paged_decode_workspace_size(...) with the same
+ * arguments, exceeds PKV_NOALLOC_SCRATCH_BYTES returns PKV_ERR_WORKSPACE and enqueues
+ * nothing. All calls on a device share the one array and it keeps the last call's contents;
+ * nothing in it has to start at zero (each call writes every partial it later reads), but
+ * calls that overlap on the GPU (other streams, other host threads) race on it: serialise
+ * them.
+ * ------------------------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+pkv_status pkv_paged_decode_attn_noalloc(const void* q, pkv_cache cache,
+                                         const int32_t* block_tables, int32_t max_blocks,
+                                         const int32_t* seq_lens, const int32_t* cu_q,
+                                         pkv_reqs reqs, int32_t num_q_heads, int32_t max_seq_len,
+                                         float scale, void* out, float* lse, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * extend_attn — new tokens against their cached context plus themselves (causal).
  * Source: vLLM blog "rocm-attention-backend", sections "ROCM_AITER_FA key innovations"
  * (extend path: chunked context attention with LSE merge, 100K+ contexts; context chunk

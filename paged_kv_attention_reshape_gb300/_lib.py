@@ -12,6 +12,7 @@ P = ctypes.c_void_p
 i32, i64, f32, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 
 PKV_OK = 0
+NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace", 4: "CUDA error",
           5: "device-side index error"}
 DEVERR = {0x1: "slot", 0x2: "block", 0x4: "reqs", 0x8: "len", 0x10: "timeout"}
@@ -35,6 +36,7 @@ SIGNATURES = [
     ("pkv_batch_classify_reorder", i32, [P, P, i32, i32, P, P, P, P, i64, P]),
     ("pkv_paged_decode_workspace_size", sz, [i32, i32, i32, i32, i32]),
     ("pkv_paged_decode_attn", i32, [P, PkvCache, P, i32, P, P, PkvReqs, i32, i32, f32, P, P, P, sz, P]),
+    ("pkv_paged_decode_attn_noalloc", i32, [P, PkvCache, P, i32, P, P, PkvReqs, i32, i32, f32, P, P, P]),
     ("pkv_extend_workspace_size", sz, [i32, i32, i32, i32, i32]),
     ("pkv_extend_attn", i32, [P, P, P, i64, P, P, PkvCache, P, i32, PkvReqs, i32, i32, i32, i32, f32,
                               P, P, P, sz, P]),

@@ -160,6 +160,27 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, 
     return out, lse
 
 
+def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, out, lse,
+                              cu_q=None, reqs: Optional[Reqs] = None, scale=None, stream=None):
+    """paged_decode_attn for callers that cannot allocate: the library uses its own fixed
+    device scratch (NOALLOC_SCRATCH_BYTES per GPU) and the caller passes out and lse."""
+    lib = _lib.load()
+    _need(q, torch.bfloat16, "q")
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    cache = make_cache(k_cache, v_cache)
+    T, Hq, D = q.shape
+    R = seq_lens.numel()
+    reqs = reqs or Reqs(max_reqs=R, batch_reqs=R)
+    _check(lib.pkv_paged_decode_attn_noalloc(_ptr(q), cache, _ptr(block_tables), block_tables.shape[1],
+                                             _ptr(seq_lens), _ptr(cu_q), reqs.c(), Hq, max_seq_len,
+                                             _scale(scale, D), _ptr(out), _ptr(lse), _stream(stream)),
+           "paged_decode_attn_noalloc")
+    return out, lse
+
+
 def extend_attn(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, max_q_len,
                 max_seq_len, reqs: Optional[Reqs] = None, chunk_budget_tokens=32768, scale=None,
                 out=None, lse=None, stream=None):

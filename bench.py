@@ -405,6 +405,44 @@ def oracle_decode_rate(b, budget_s=15.0, host=None):
                        f"{t_total:.1f} s")
 
 
+# ---- reduced cases for ncu captures --------------------------------------------------------------
+
+def profile_case(pkv, args):
+    """A few launches of one kernel on a reduced case whose inputs still exceed L2 (129 MB), so
+    DRAM counters mean something while the capture stays small (well under 1 GB on the device)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream()
+    if args.profile == "decode":
+        # 64 sequences of the decode workload's shape: ~330 MB of KV per launch
+        b = gen.decode_batch(64, 2000, 3000, Hq=64, Hkv=4, D=128, seed=1, device=dev)
+        maxs = max(b.seq_lens_list)
+        ws = torch.empty(max(16, pkv.paged_decode_workspace_size(b.R, 64, 4, 128, maxs)), dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.paged_decode_attn(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, maxs,
+                                           cu_q=b.cu_q, workspace=ws)
+        what = f"decode B=64 kv_bytes={sum(b.seq_lens_list) * 4 * 128 * 4}"
+    elif args.profile == "prefill":
+        b = gen.prefill_batch([4096, 4096], Hq=64, Hkv=8, D=128, seed=5, device=dev)
+        fn = lambda: pkv.varlen_prefill_attn(b.q, b.k_new, b.v_new, b.cu_q, 4096)
+        what = "prefill 2 x 4096, Hq 64 / Hkv 8"
+    elif args.profile == "extend":
+        b = gen.extend_batch([512, 512], [16000, 16000], Hq=64, Hkv=8, D=128, seed=3, device=dev)
+        fn = lambda: pkv.extend_attn(b.q, b.k_new, b.v_new, b.cu_q, b.seq_lens, b.k_cache, b.v_cache,
+                                     b.block_tables, 512, max(b.seq_lens_list))
+        what = "extend 2 x (16000 cached + 512 new)"
+    else:
+        layers = gen.write_pack_layers(4, 10000, Hkv=8, D=128, seed=4, device=dev)
+        def fn():
+            for L in layers:
+                pkv.kv_cache_write(L.key, L.value, L.slot_mapping, L.k_cache, L.v_cache)
+                pkv.kv_block_pack(L.k_cache, L.v_cache, L.block_ids)
+        what = "write + pack, 4 layers x 10000 tokens"
+    for _ in range(args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(f"profile case done: {what}, {args.steps} launches, device errors {pkv.device_errors()}")
+
+
 # ---- main ---------------------------------------------------------------------------------------
 
 def main():
@@ -415,6 +453,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["decode", "prefill", "extend", "write_pack"], default=None,
+                    help="run a reduced case of one kernel --steps times for an ncu capture; prints "
+                         "a one-line summary, no benchmark line")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     steps, warmup = args.steps, max(3, args.warmup)
@@ -444,6 +485,8 @@ def main():
 
     import paged_kv_attention_reshape_gb300 as pkv
     pkv.load()
+    if args.profile:
+        return profile_case(pkv, args)
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")

@@ -363,8 +363,8 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   CUtensorMap tq, tk, tv, tck, tcv;
   std::memset(&tck, 0, sizeof tck);
   std::memset(&tcv, 0, sizeof tcv);
-  if (!encode_rows(&tq, q, num_tokens, Hq, D, 64) || !encode_rows(&tk, k, num_tokens, Hkv, D, 64) ||
-      !encode_rows(&tv, v, num_tokens, Hkv, D, 64))
+  if (!encode_rows(&tq, q, num_tokens, Hq, D, 128) || !encode_rows(&tk, k, num_tokens, Hkv, D, 128) ||
+      !encode_rows(&tv, v, num_tokens, Hkv, D, 128))
     return PKV_ERR_CUDA;
   if (cache != nullptr &&
       (!encode_cache(&tck, cache->k, *cache) || !encode_cache(&tcv, cache->v, *cache)))

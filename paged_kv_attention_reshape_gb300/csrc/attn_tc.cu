@@ -282,7 +282,9 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
           tc::st16(tmem + lane_off + scol(slot) + c * 16, pk);
         }
         l = l * alpha + rs;
-        if (alpha != 1.f && j > 0) {
+        // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole
+        // warp takes the branch when any of its rows needs it (alpha is 1 for the others).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O of this row is quiescent: the previous P V product finished before S(j) did
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {

@@ -243,43 +243,58 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         if (!tc_wait_warp(&s_full[slot], sc & 1, &s_abort, p.err)) { ok = false; break; }
         ++sc;
         tc::fence_after_sync();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld32(tmem + lane_off + scol(slot) + c * 32, s[c]);
-        tc::wait_ld();
         // valid keys of this row in tile j: columns [0, kv) (context) or causal (new)
         int kv;
         if (j < it.nct) kv = min(128, it.C - j * 128);
         else kv = min(128, qi - (j - it.nct) * 128 + 1);
+        const bool full = __all_sync(0xffffffffu, kv >= 128);
+        const uint32_t srow = tmem + lane_off + scol(slot);
+        // pass 1: row max of the raw scores (the scale is positive, so it commutes with max)
         float mx = -CUDART_INF_F;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc::ld32(srow + c * 32, v);
+          tc::wait_ld();
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float v = (c * 32 + e < kv) ? __uint_as_float(s[c][e]) * p.scale_log2 : -CUDART_INF_F;
-            s[c][e] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e < kv) mx = fmaxf(mx, __uint_as_float(v[e]));
           }
+        }
+        mx = mx * p.scale_log2;  // -inf stays -inf
         float alpha = 1.f;
         if (mx > m + 8.f || m == -CUDART_INF_F) {  // lazy rescale: only when the max really grows
           const float m_new = fmaxf(m, mx);
           if (m_new != -CUDART_INF_F) {
-            alpha = (m == -CUDART_INF_F) ? 0.f : fast_exp2(m - m_new);
+            alpha = (m == -CUDART_INF_F) ? 0.f : ex2_approx(m - m_new);
             m = m_new;
           }
         }
+        // pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs over the first half of S
+        const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
         float rs = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc::ld32(srow + c * 32, v);
+          tc::wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = m == -CUDART_INF_F ? 0.f : fast_exp2(__uint_as_float(s[c][e]) - m);
-            const float p1 = m == -CUDART_INF_F ? 0.f : fast_exp2(__uint_as_float(s[c][e + 1]) - m);
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, neg_m));
+            if (!full) {
+              p0 = (c * 32 + e < kv) ? p0 : 0.f;
+              p1 = (c * 32 + e + 1 < kv) ? p1 : 0.f;
+            }
             rs += p0 + p1;
             pk[e / 2] = pack_bf16(p0, p1);
           }
-          tc::st16(tmem + lane_off + scol(slot) + c * 16, pk);
+          tc::st16(srow + c * 16, pk);
         }
         l = l * alpha + rs;
         // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole

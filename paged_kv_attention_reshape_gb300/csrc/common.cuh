@@ -128,5 +128,11 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
 }
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// The hardware base-2 exponential (MUFU), flushing denormal results to zero; 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace pkv

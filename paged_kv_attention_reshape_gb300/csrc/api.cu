@@ -119,21 +119,6 @@ pkv_status check_reqs(const pkv_reqs& r) {
 
 pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
-// Split-KV shape for decode: enough CTAs to fill the GPU a few times over, each split at
-// least 256 tokens, split length a multiple of the block size.
-void decode_split(int max_reqs, int Hkv, int max_seq_len, int sms, int* split_tokens,
-                  int* max_splits) {
-  const int64_t units = static_cast<int64_t>(max_reqs) * Hkv;
-  const int64_t target = static_cast<int64_t>(sms) * 8;
-  int splits = units > 0 ? static_cast<int>((target + units - 1) / units) : 1;
-  const int cap = max(1, (max_seq_len + 255) / 256);
-  splits = max(1, min(splits, cap));
-  int st = (max_seq_len + splits - 1) / splits;
-  st = max(16, (st + 15) / 16 * 16);
-  *split_tokens = st;
-  *max_splits = max(1, (max_seq_len + st - 1) / st);
-}
-
 }  // namespace
 
 int num_sms() {
@@ -250,12 +235,10 @@ pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_le
 
 size_t pkv_paged_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t max_seq_len) {
-  if (max_reqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0) return 0;
-  int st, ms;
-  decode_split(max_reqs, num_kv_heads, max_seq_len, num_sms(), &st, &ms);
-  if (ms <= 1) return 0;
-  const size_t n = static_cast<size_t>(max_reqs) * num_q_heads * ms;
-  return n * head_dim * sizeof(float) + n * sizeof(float);
+  (void)max_reqs;
+  (void)max_seq_len;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_q_heads % num_kv_heads) return 0;
+  return decode_workspace_bytes(num_q_heads / num_kv_heads, head_dim);
 }
 
 pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
@@ -293,19 +276,11 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   p.num_blocks = cache.num_blocks;
   p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f;
-  decode_split(reqs.max_reqs, cache.num_kv_heads, max_seq_len, num_sms(), &p.split_tokens,
-               &p.max_splits);
-  if (p.max_splits > 1) {
-    const size_t need = pkv_paged_decode_workspace_size(reqs.max_reqs, num_q_heads,
-                                                        cache.num_kv_heads, cache.head_dim,
-                                                        max_seq_len);
-    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
-      return PKV_ERR_WORKSPACE;
-    const size_t n = static_cast<size_t>(reqs.max_reqs) * num_q_heads * p.max_splits;
-    p.ws_o = static_cast<float*>(workspace);
-    p.ws_lse = p.ws_o + n * cache.head_dim;
-  }
-  if (p.max_splits > 65535) return PKV_ERR_UNSUPPORTED;
+  const size_t need = decode_workspace_bytes(p.G, cache.head_dim);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  p.ws_part = static_cast<float*>(workspace);
+  p.ws_pre = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                        decode_workspace_pre_offset(p.G, cache.head_dim));
   CUtensorMap tk, tv;
   if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
   int launches = 0;

@@ -29,10 +29,8 @@ struct DecodeParams {
   int64_t num_blocks;
   int32_t max_seq_len;
   float scale_log2;      // softmax scale * log2(e)
-  int32_t split_tokens;  // tokens per split (multiple of the block size)
-  int32_t max_splits;
-  float* ws_o;           // [max_reqs, Hq, max_splits, D] normalised partial outputs
-  float* ws_lse;         // [max_reqs, Hq, max_splits] natural-log partial LSE
+  float* ws_part;        // [grid][2][G][D + 4] partials of units cut at CTA share edges
+  int32_t* ws_pre;       // [set size + 1] block prefix of the set's units (for the merge)
 };
 
 // Extend and prefill share one kernel; prefill is the case without cached context.
@@ -84,6 +82,9 @@ cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* se
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int D, cudaStream_t stream, int* launches);
 int decode_smem_bytes(int D);
+int decode_grid();
+size_t decode_workspace_bytes(int G, int D);
+size_t decode_workspace_pre_offset(int G, int D);
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
 // (ignored for prefill).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -87,9 +87,11 @@ def test_host_checks_reject_bad_arguments_without_a_gpu(lib):
 
 
 def test_decode_workspace_query_is_host_only(lib):
-    assert lib.pkv_paged_decode_workspace_size(0, 64, 4, 128, 3000) == 0
-    n = lib.pkv_paged_decode_workspace_size(4, 8, 2, 64, 200)
-    assert n >= 0
+    # partials for two cut units per CTA plus the set's block prefix: a few MB, independent of
+    # the batch; invalid head counts give 0
+    n = lib.pkv_paged_decode_workspace_size(256, 64, 4, 128, 3000)
+    assert 0 < n <= 32 << 20
+    assert lib.pkv_paged_decode_workspace_size(4, 8, 3, 64, 200) == 0
 
 
 def test_product_path_has_no_fallback():

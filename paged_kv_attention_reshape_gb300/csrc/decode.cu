@@ -6,22 +6,23 @@
 // sequence computed apart are combined with the LSE merge of the extend path ("Processing
 // details: extend path").
 //
-// Design (HBM-bound, persistent):
+// Design (HBM-bound, persistent, one worker per warp):
 //   * the work is the list of 16-token KV blocks of every (sequence, KV head) unit of the set;
-//     a fixed grid of CTAs (two per SM) takes equal, contiguous shares of that list, so every
-//     CTA streams the same number of bytes and no wave tail is left; a share may start or end
-//     inside a unit;
-//   * a producer warp streams the share's blocks with TMA (128-byte swizzle, one box per
-//     64-wide half of head_dim and K/V) into an NS-deep ring of shared-memory stages; block
-//     table entries are fetched 32 at a time, one batch ahead;
-//   * four consumer warps take blocks round-robin. The G = Hq/Hkv query heads of the unit's
-//     KV head share every K/V tile: they sit on the M dimension of the warp-level bf16 MMA
-//     (m16n8k16, fp32 accumulate), padded to 16 rows. Each warp keeps its own online-softmax
-//     state (running max, sum, O) in registers; exp2 runs with the scale folded in;
-//   * at the end of each unit piece the warps' states are merged in shared memory. A piece that
-//     covers its whole unit writes out/lse; a piece cut at a share edge writes an fp32 partial
-//     (normalised O and natural-log LSE), and decode_merge_kernel folds the pieces of each cut
-//     unit with the LSE merge (at most two partial slots per CTA).
+//     every warp of a fixed grid (two CTAs of four warps per SM) is an independent worker that
+//     takes an equal, contiguous share of that list, so every worker streams the same number
+//     of bytes and no wave tail is left; a share may start or end inside a unit;
+//   * a worker streams its blocks itself: lane 0 issues TMA loads (128-byte swizzle, one box
+//     per 64-wide half of head_dim and K/V) into the worker's own ring of NSW stages, NSW
+//     blocks ahead of the math; block-table entries come 32 at a time in one coalesced load,
+//     one batch ahead;
+//   * the G = Hq/Hkv query heads of the unit's KV head share every K/V tile: they sit on the M
+//     dimension of the warp-level bf16 MMA (m16n8k16, fp32 accumulate), padded to 16 rows; the
+//     online-softmax state (running max, sum, O) stays in registers; exp2 runs with the scale
+//     folded in;
+//   * a piece that covers its whole unit writes out/lse from registers; a piece cut at a share
+//     edge writes an fp32 partial (normalised O and natural-log LSE), and decode_merge_kernel
+//     folds the pieces of each cut unit with the LSE merge (at most two partial slots per
+//     worker). No shared-memory combine, no block-wide barrier after the prologue.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -31,28 +32,21 @@ namespace pkv {
 
 template <int D>
 struct DecodeCfg {
-  static constexpr int NW = 4;                        // consumer warps
-  // Ring stages. A multiple of NW, so that every use of a stage belongs to the same consumer
-  // warp and that warp waits on the stage's phases in order: an mbarrier parity wait cannot
-  // tell phase u from phase u + 2, so a warp must never wait on use u + 1 of a stage while
-  // use u (someone else's) may still be in flight.
-  static constexpr int NS = 4;
+  static constexpr int NW = 4;                        // worker warps per CTA
+  static constexpr int NSW = 2;                       // ring stages per worker
   static constexpr int BS = 16;                       // tokens per block
   static constexpr int HALVES = D / 64;               // 64-element (128-byte) column halves
   static constexpr int TILE_BYTES = BS * D * 2;       // one block of K (or V) for one head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
   static constexpr int Q_BYTES = 16 * D * 2;
-  static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int MAXR = 1024;       // requests per set handled on device
-  static constexpr int MIN_BLOCKS = 8;    // smallest share (blocks) a CTA is given
-  static constexpr int COMBINE_BYTES = NW * 16 * (D + 2) * 4;
-  static constexpr int RING_OFF = 0;
-  static constexpr int Q_OFF = NS * STAGE_BYTES;
-  static constexpr int COMB_OFF = Q_OFF + 2 * Q_BYTES;
-  static constexpr int TAB_OFF = COMB_OFF + COMBINE_BYTES;  // s_pre[MAXR+1], s_ctx, s_r, s_row
+  static constexpr int THREADS = NW * 32;
+  static constexpr int MAXR = 1024;     // requests per set handled on device
+  static constexpr int MIN_BLOCKS = 8;  // smallest share (blocks) a worker is given
+  static constexpr int RING_OFF = 0;    // [NW][NSW][K | V]
+  static constexpr int Q_OFF = NW * NSW * STAGE_BYTES;   // [NW][half][16][64]
+  static constexpr int TAB_OFF = Q_OFF + NW * Q_BYTES;   // s_pre[MAXR+1], s_ctx, s_r, s_row
   static constexpr int BAR_OFF = TAB_OFF + (4 * MAXR + 4) * 4;
-  static constexpr int SMEM = 1024 + BAR_OFF + 2 * NS * 8;
-  static_assert(NS % NW == 0, "each ring stage must belong to one consumer warp");
+  static constexpr int SMEM = 1024 + BAR_OFF + NW * NSW * 8;
 };
 
 // Resolve the request set: [begin, begin + n) of `order` (or of the identity).
@@ -67,23 +61,23 @@ __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, i
   }
 }
 
-// First block of CTA c's share: shares are [c*TB/nc, (c+1)*TB/nc).
-__device__ __forceinline__ int64_t share_start(int c, int64_t TB, int nc) {
-  return static_cast<int64_t>(c) * TB / nc;
+// First block of worker w's share: shares are [w*TB/nw, (w+1)*TB/nw).
+__device__ __forceinline__ int64_t share_start(int w, int64_t TB, int nw) {
+  return static_cast<int64_t>(w) * TB / nw;
 }
-// The CTA whose share holds block b.
-__device__ __forceinline__ int share_of(int64_t b, int64_t TB, int nc) {
-  int lo = 0, hi = nc - 1;
+// The worker whose share holds block b.
+__device__ __forceinline__ int share_of(int64_t b, int64_t TB, int nw) {
+  int lo = 0, hi = nw - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (share_start(mid, TB, nc) <= b) lo = mid; else hi = mid - 1;
+    if (share_start(mid, TB, nw) <= b) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
-// CTAs that get work: at least MIN_BLOCKS blocks each.
-__device__ __forceinline__ int active_ctas(int64_t TB, int grid, int min_blocks) {
+// Workers that get work: at least MIN_BLOCKS blocks each.
+__device__ __forceinline__ int active_workers(int64_t TB, int workers, int min_blocks) {
   const int64_t want = (TB + min_blocks - 1) / min_blocks;
-  return static_cast<int>(want < grid ? (want > 0 ? want : 1) : grid);
+  return static_cast<int>(want < workers ? (want > 0 ? want : 1) : workers);
 }
 
 // A piece of a unit (set position i, KV head kh): its local blocks [lo, hi).
@@ -135,18 +129,6 @@ struct PieceIter {
   }
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void consumers_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
     const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
@@ -154,17 +136,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
   using C = DecodeCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem + C::RING_OFF;
-  uint8_t* sQ = smem + C::Q_OFF;  // two buffers [half][16][64]
-  float* comb = reinterpret_cast<float*>(smem + C::COMB_OFF);
   int* s_pre = reinterpret_cast<int*>(smem + C::TAB_OFF);
   int* s_ctx = s_pre + C::MAXR + 1;
   int* s_r = s_ctx + C::MAXR;
   int* s_row = s_r + C::MAXR;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* empty = full + C::NS;
   __shared__ int s_scan[C::THREADS / 32];
-  __shared__ int s_fail;  // a consumer warp gave up waiting (all consumers then stop together)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.Hkv, G = p.G;
@@ -225,126 +201,120 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
   if (blockIdx.x == 0) {
     for (int i = tid; i <= n; i += C::THREADS) p.ws_pre[i] = s_pre[i];
   }
-  const int nc = active_ctas(TB, gridDim.x, C::MIN_BLOCKS);
-  if (TB == 0 || static_cast<int>(blockIdx.x) >= nc) return;
-  const int64_t b0 = share_start(blockIdx.x, TB, nc), b1 = share_start(blockIdx.x + 1, TB, nc);
+  if (TB == 0) return;
+
+  // ---- this warp is worker wk with share [b0, b1) ----
+  const int nwk = active_workers(TB, gridDim.x * C::NW, C::MIN_BLOCKS);
+  const int wk = blockIdx.x * C::NW + warp;
+  if (wk >= nwk) return;  // warp-uniform; nothing below synchronises across warps
+  const int64_t b0 = share_start(wk, TB, nwk), b1 = share_start(wk + 1, TB, nwk);
   if (b0 >= b1) return;
 
-  if (tid == 0) {
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    s_fail = 0;
+  uint8_t* ring = smem + C::RING_OFF + warp * C::NSW * C::STAGE_BYTES;
+  uint8_t* sQ = smem + C::Q_OFF + warp * C::Q_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * C::NSW;
+  if (lane == 0) {
+    for (int s = 0; s < C::NSW; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
-  __syncthreads();
+  __syncwarp();
 
-  PieceIter it;
-  it.start(s_pre, n, Hkv, b0, b1);
-  Piece pc;
-
-  if (warp == C::NW) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+  // ---- load cursor: walks the share block by block and issues the TMA loads ----
+  PieceIter lit;
+  lit.start(s_pre, n, Hkv, b0, b1);
+  Piece lpc{0, 0, 0, 0};
+  int lj = 0;                 // next block (local index) of lpc to load
+  bool lhave = false;         // lpc valid
+  int lbatch = 0, lnext = 0;  // this lane's table entries: block lpc.lo + lbase + lane (and +32)
+  int lbase = 0;
+  const int32_t* ltable = nullptr;
+  uint32_t issued = 0;        // blocks whose loads were issued
+  auto fetch_entries = [&](int base) {
+    const int nb = lpc.hi - lpc.lo;
+    lbatch = (base + lane < nb) ? ltable[base + lane] : 0;
+    lnext = (base + 32 + lane < nb) ? ltable[base + 32 + lane] : 0;
+  };
+  // Issue the next block of the share into `stage`; false when the share is exhausted.
+  auto issue_next = [&](int stage) -> bool {
+    if (!lhave || lj == lpc.hi - lpc.lo) {
+      if (!lit.next(lpc)) return false;
+      lhave = true;
+      lj = 0;
+      lbase = 0;
+      ltable = p.block_tables + static_cast<int64_t>(s_r[lpc.i]) * p.max_blocks + lpc.lo;
+      fetch_entries(0);
+    } else if (lj == lbase + 32) {
+      lbase += 32;
+      lbatch = lnext;
+      lnext = (lbase + 32 + lane < lpc.hi - lpc.lo) ? ltable[lbase + 32 + lane] : 0;
     }
-    uint32_t g = 0;  // blocks issued by this CTA
-    bool ok = true;
-    while (ok && it.next(pc)) {
-      const int32_t* table = p.block_tables + static_cast<int64_t>(s_r[pc.i]) * p.max_blocks + pc.lo;
-      const int nblk = pc.hi - pc.lo;
-      int nxt = lane < nblk ? table[lane] : 0;
-      for (int jb = 0; jb < nblk && ok; jb += 32) {
-        int cur = nxt;
-        nxt = (jb + 32 + lane < nblk) ? table[jb + 32 + lane] : 0;
-        if (jb + lane < nblk && (cur < 0 || cur >= p.num_blocks)) {
-          flag_error(p.err, PKV_DEVERR_BLOCK);
-          cur = 0;
-        }
-        const int nb = min(32, nblk - jb);
-        for (int k = 0; k < nb; ++k, ++g) {
-          const int blk = __shfl_sync(0xffffffffu, cur, k);
-          const int s = g % C::NS;
-          if (lane == 0) {
-            if (g >= C::NS) ok = mbar_wait(&empty[s], ((g / C::NS) - 1) & 1, p.err);
-            if (ok) {
-              uint8_t* sK = ring + s * C::STAGE_BYTES;
-              uint8_t* sV = sK + C::TILE_BYTES;
-              mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+    int blk = __shfl_sync(0xffffffffu, lbatch, lj - lbase);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (lane == 0) flag_error(p.err, PKV_DEVERR_BLOCK);
+      blk = 0;
+    }
+    if (lane == 0) {
+      uint8_t* sK = ring + stage * C::STAGE_BYTES;
+      uint8_t* sV = sK + C::TILE_BYTES;
+      mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
-              for (int h = 0; h < C::HALVES; ++h) {
-                tma_load_4d(sK + h * 2048, &tm_k, &full[s], 0, pc.kh * C::HALVES + h, 0, blk);
-                tma_load_4d(sV + h * 2048, &tm_v, &full[s], 0, pc.kh * C::HALVES + h, 0, blk);
-              }
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-        }
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_4d(sK + h * 2048, &tm_k, &full[stage], 0, lpc.kh * C::HALVES + h, 0, blk);
+        tma_load_4d(sV + h * 2048, &tm_v, &full[stage], 0, lpc.kh * C::HALVES + h, 0, blk);
       }
     }
-    return;
-  }
-
-  // ---------------- consumers ----------------
-  const int ctid = tid;  // 0 .. NW*32-1
-  auto load_q = [&](const Piece& q, int buf) {
-    // 16 rows (query heads kh*G .. kh*G+G-1, zero padded) x D into buffer `buf`, laid out
-    // [half][16][64] with the 128-byte swizzle the ldmatrix addressing below expects
-    const int64_t row = s_row[q.i];
-    uint8_t* dst = sQ + buf * C::Q_BYTES;
-    for (int c = ctid; c < 16 * (D / 8); c += C::NW * 32) {
-      const int gg = c / (D / 8), chunk = c % (D / 8);
-      const bool valid = gg < G;
-      const __nv_bfloat16* src = p.q + (row * p.Hq + q.kh * G + (valid ? gg : 0)) * D + chunk * 8;
-      cp_async16(dst + (chunk / 8) * 2048 + sw128(gg, chunk % 8), src, valid);
-    }
-    cp_async_commit();
+    ++lj;
+    ++issued;
+    return true;
   };
+  bool more = true;
+#pragma unroll
+  for (int s = 0; s < C::NSW; ++s)
+    if (more) more = issue_next(s);
 
-  Piece cur_pc, next_pc;
-  bool have = it.next(cur_pc);
-  if (have) load_q(cur_pc, 0);
-  bool have_next = have && it.next(next_pc);
-  uint32_t g = 0;  // blocks consumed by this CTA (all warps)
-  int k = 0;
+  // ---- compute cursor ----
+  PieceIter cit;
+  cit.start(s_pre, n, Hkv, b0, b1);
+  Piece pc;
+  uint32_t t = 0;  // blocks consumed by this worker
   bool ok = true;
-  while (have && ok) {
-    if (have_next) {
-      load_q(next_pc, (k + 1) & 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  const int r0 = lane >> 2;  // fragment rows r0 and r0 + 8
+  while (ok && cit.next(pc)) {
+    // Q tile of the piece: 16 rows (query heads kh*G .. kh*G+G-1, zero padded) x D, laid out
+    // [half][16][64] with the 128-byte swizzle the ldmatrix addressing expects
+    const int64_t row = s_row[pc.i];
+    for (int c = lane; c < 16 * (D / 8); c += 32) {
+      const int gg = c / (D / 8), chunk = c % (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (gg < G) v = *reinterpret_cast<const uint4*>(p.q + (row * p.Hq + pc.kh * G + gg) * D + chunk * 8);
+      *reinterpret_cast<uint4*>(sQ + (chunk / 8) * 2048 + sw128(gg, chunk % 8)) = v;
     }
-    consumers_sync(C::NW * 32);  // Q of this piece landed for every thread; comb is free
+    __syncwarp();
     uint32_t qa[D / 16][4];
     {
-      const uint32_t qbase = smem_u32(sQ + (k & 1) * C::Q_BYTES);
+      const uint32_t qbase = smem_u32(sQ);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         ldsm_x4(qbase + (ks / 4) * 2048 + sw128(lane & 15, (ks % 4) * 2 + (lane >> 4)), qa[ks][0], qa[ks][1],
                 qa[ks][2], qa[ks][3]);
     }
-    const int ctx = s_ctx[cur_pc.i];
-    const int nblk = cur_pc.hi - cur_pc.lo;
-    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows lane/4 and lane/4 + 8 (log2 units)
+    const int ctx = s_ctx[pc.i];
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows r0 and r0 + 8 (log2 units)
     float l_run[2] = {0.f, 0.f};
     float o[D / 8][4];
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // this warp's blocks of the piece: global block numbers g + jj with (g + jj) % NW == warp
-    for (int jj = (warp - static_cast<int>(g % C::NW) + C::NW) % C::NW; jj < nblk; jj += C::NW) {
-      const uint32_t gb = g + jj;
-      const int s = gb % C::NS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (gb / C::NS) & 1, p.err))) {
-        s_fail = 1;
+    for (int j = pc.lo; j < pc.hi; ++j, ++t) {
+      const int s = t % C::NSW;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / C::NSW) & 1, p.err))) {
+        ok = false;
         break;
       }
       uint8_t* sK = ring + s * C::STAGE_BYTES;
       uint8_t* sV = sK + C::TILE_BYTES;
-      const int valid = min(C::BS, ctx - (cur_pc.lo + jj) * C::BS);  // tokens of this block
+      const int valid = min(C::BS, ctx - j * C::BS);  // tokens of this block
       if (valid < C::BS) {
         // zero the V rows past the end so that P = 0 there cannot meet a non-finite value
         for (int c = lane; c < (C::BS - valid) * C::HALVES * 8; c += 32) {
@@ -421,90 +391,55 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
         mma_16816(o[2 * nd], pa, b0r, b1r);
         mma_16816(o[2 * nd + 1], pa, b2r, b3r);
       }
-      if (valid < C::BS) fence_proxy_async_smem();  // generic writes before TMA reuses the stage
+      // the stage's reads (and any zeroing) are done: refill it with the block NSW ahead
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (more) more = issue_next(s);
     }
-    g += nblk;
+    if (!ok) break;
+    // ---- the piece's result ----
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
     }
-    // ---- merge the warps' states of this piece ----
-    float* cm = comb;                 // [NW][16] max
-    float* cl = cm + C::NW * 16;      // [NW][16] sum
-    float* co = cl + C::NW * 16;      // [NW][16][D] unnormalised O
-    {
-      const int r0 = lane >> 2;
-      if ((lane & 3) == 0) {
-        cm[warp * 16 + r0] = m_run[0];
-        cm[warp * 16 + r0 + 8] = m_run[1];
-        cl[warp * 16 + r0] = l_run[0];
-        cl[warp * 16 + r0 + 8] = l_run[1];
-      }
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        const int col = i * 8 + 2 * (lane & 3);
-        *reinterpret_cast<float2*>(co + (warp * 16 + r0) * D + col) = make_float2(o[i][0], o[i][1]);
-        *reinterpret_cast<float2*>(co + (warp * 16 + r0 + 8) * D + col) = make_float2(o[i][2], o[i][3]);
-      }
-    }
-    // every consumer warp reaches this barrier, also after a timeout, so none is left waiting
-    consumers_sync(C::NW * 32);
     const int unit_blocks = (ctx + C::BS - 1) / C::BS;
-    const bool whole = cur_pc.lo == 0 && cur_pc.hi == unit_blocks;
-    // partial slot: 0 for a piece that starts this CTA's share inside its unit, else 1
-    const int64_t piece_first = s_pre[cur_pc.i] + static_cast<int64_t>(cur_pc.kh) * unit_blocks + cur_pc.lo;
-    const int slot = (piece_first == b0 && cur_pc.lo != 0) ? 0 : 1;
-    const int64_t row = s_row[cur_pc.i];
-    for (int c = ctid; c < G * (D / 8); c += C::NW * 32) {
-      const int gg = c / (D / 8), cg = (c % (D / 8)) * 8;
-      float M = -CUDART_INF_F;
+    const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
+    // partial slot: 0 for a piece that starts this worker's share inside its unit, else 1
+    const int64_t piece_first = s_pre[pc.i] + static_cast<int64_t>(pc.kh) * unit_blocks + pc.lo;
+    const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) M = fmaxf(M, cm[w * 16 + gg]);
-      float L = 0.f, acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-      for (int w = 0; w < C::NW; ++w) {
-        const float mw = cm[w * 16 + gg];
-        const float sw = (mw == -CUDART_INF_F) ? 0.f : ex2_approx(mw - M);
-        L += cl[w * 16 + gg] * sw;
-        const float4 a = *reinterpret_cast<const float4*>(co + (w * 16 + gg) * D + cg);
-        const float4 b = *reinterpret_cast<const float4*>(co + (w * 16 + gg) * D + cg + 4);
-        acc[0] += a.x * sw; acc[1] += a.y * sw; acc[2] += a.z * sw; acc[3] += a.w * sw;
-        acc[4] += b.x * sw; acc[5] += b.y * sw; acc[6] += b.z * sw; acc[7] += b.w * sw;
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
-      const int h = cur_pc.kh * G + gg;
+    for (int h = 0; h < 2; ++h) {
+      const int gg = r0 + 8 * h;
+      if (gg >= G) continue;
+      const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+      const float lse = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
+      const int hq = pc.kh * G + gg;
       if (whole) {
-        uint4 ov;
-        ov.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-        ov.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-        ov.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-        ov.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(p.out + (row * p.Hq + h) * D + cg) = ov;
-        if (p.lse && cg == 0) p.lse[row * p.Hq + h] = lse;
+        __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + 2 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+          *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+        if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse;
       } else {
-        float* dst = p.ws_part + ((static_cast<int64_t>(blockIdx.x) * 2 + slot) * G + gg) * (D + 4);
-        reinterpret_cast<float4*>(dst)[cg / 4] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-        reinterpret_cast<float4*>(dst)[cg / 4 + 1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-        if (cg == 0) dst[D] = lse;
+        float* dst = p.ws_part + ((static_cast<int64_t>(wk) * 2 + slot) * G + gg) * (D + 4);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+          *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+        if ((lane & 3) == 0) dst[D] = lse;
       }
     }
-    consumers_sync(C::NW * 32);
-    ok = s_fail == 0;
-    cur_pc = next_pc;
-    have = have_next;
-    if (have) have_next = it.next(next_pc);
-    ++k;
+  }
+  // after a timeout, wait (bounded) for this worker's loads still in flight before exiting
+  for (; t < issued; ++t) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[t % C::NSW], (t / C::NSW) & 1, p.err))) break;
   }
 }
 
 // One warp per (unit, query head): units with no blocks get out = 0, lse = -inf; units cut
-// across CTA shares get the LSE merge of their pieces.
+// across worker shares get the LSE merge of their pieces.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int grid) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int workers) {
   using C = DecodeCfg<D>;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -528,26 +463,26 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
     return;
   }
   const int64_t TB = p.ws_pre[n];
-  const int nc = active_ctas(TB, grid, C::MIN_BLOCKS);
+  const int nwk = active_workers(TB, workers, C::MIN_BLOCKS);
   const int64_t first = p.ws_pre[i] + static_cast<int64_t>(kh) * nb;
-  const int c0 = share_of(first, TB, nc), c1 = share_of(first + nb - 1, TB, nc);
-  if (c0 == c1) return;  // written whole by the decode kernel
+  const int w0 = share_of(first, TB, nwk), w1 = share_of(first + nb - 1, TB, nwk);
+  if (w0 == w1) return;  // written whole by the decode kernel
   float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c) {
-    const float* src = p.ws_part + ((static_cast<int64_t>(c) * 2 + (c == c0 ? 1 : 0)) * G + gg) * (D + 4);
+  for (int w = w0; w <= w1; ++w) {
+    const float* src = p.ws_part + ((static_cast<int64_t>(w) * 2 + (w == w0 ? 1 : 0)) * G + gg) * (D + 4);
     M = fmaxf(M, src[D]);
   }
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float W = 0.f;
-  for (int c = c0; c <= c1; ++c) {
-    const float* src = p.ws_part + ((static_cast<int64_t>(c) * 2 + (c == c0 ? 1 : 0)) * G + gg) * (D + 4);
+  for (int w = w0; w <= w1; ++w) {
+    const float* src = p.ws_part + ((static_cast<int64_t>(w) * 2 + (w == w0 ? 1 : 0)) * G + gg) * (D + 4);
     const float l = src[D];
-    const float w = (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
-    W += w;
+    const float wt = (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
+    W += wt;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += w * src[lane * PER + e];
+    for (int e = 0; e < PER; ++e) acc[e] += wt * src[lane * PER + e];
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
 #pragma unroll
@@ -558,14 +493,13 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
 
 int decode_grid() { return 2 * num_sms(); }
 
-// Partials: [grid][2 slots][G][D + 4] floats (O, then the LSE at index D; rows padded to 16
+// Partials: [workers][2 slots][G][D + 4] floats (O, then the LSE at index D; rows padded to 16
 // bytes), then the set's block prefix [MAXR + 1] ints for the merge kernel.
 size_t decode_workspace_bytes(int G, int D) {
-  return static_cast<size_t>(decode_grid()) * 2 * G * (D + 4) * sizeof(float) +
-         static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
+  return decode_workspace_pre_offset(G, D) + static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
 }
 size_t decode_workspace_pre_offset(int G, int D) {
-  return static_cast<size_t>(decode_grid()) * 2 * G * (D + 4) * sizeof(float);
+  return static_cast<size_t>(decode_grid()) * DecodeCfg<128>::NW * 2 * G * (D + 4) * sizeof(float);
 }
 
 template <int D>
@@ -581,7 +515,7 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = static_cast<int64_t>(min(p.max_reqs, C::MAXR)) * p.Hq;
-  decode_merge_kernel<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p, grid);
+  decode_merge_kernel<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p, grid * C::NW);
   *launches += 1;
   return cudaGetLastError();
 }

@@ -238,7 +238,7 @@ size_t pkv_paged_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, in
   (void)max_reqs;
   (void)max_seq_len;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_q_heads % num_kv_heads) return 0;
-  return decode_workspace_bytes(num_q_heads / num_kv_heads, head_dim);
+  return decode_workspace_bytes(num_q_heads, num_kv_heads, head_dim);
 }
 
 pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
@@ -276,11 +276,11 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   p.num_blocks = cache.num_blocks;
   p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const size_t need = decode_workspace_bytes(p.G, cache.head_dim);
+  const size_t need = decode_workspace_bytes(p.Hq, p.Hkv, cache.head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   p.ws_part = static_cast<float*>(workspace);
   p.ws_pre = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
-                                        decode_workspace_pre_offset(p.G, cache.head_dim));
+                                        decode_workspace_pre_offset(p.Hq, p.Hkv, cache.head_dim));
   CUtensorMap tk, tv;
   if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
   int launches = 0;

@@ -6,23 +6,26 @@
 // sequence computed apart are combined with the LSE merge of the extend path ("Processing
 // details: extend path").
 //
-// Design (HBM-bound, persistent, one worker per warp):
-//   * the work is the list of 16-token KV blocks of every (sequence, KV head) unit of the set;
-//     every warp of a fixed grid (two CTAs of four warps per SM) is an independent worker that
-//     takes an equal, contiguous share of that list, so every worker streams the same number
-//     of bytes and no wave tail is left; a share may start or end inside a unit;
-//   * a worker streams its blocks itself: lane 0 issues TMA loads (128-byte swizzle, one box
-//     per 64-wide half of head_dim and K/V) into the worker's own ring of NSW stages, NSW
-//     blocks ahead of the math; block-table entries come 32 at a time in one coalesced load,
-//     one batch ahead;
-//   * the G = Hq/Hkv query heads of the unit's KV head share every K/V tile: they sit on the M
+// Design (HBM-bound, persistent, one KV head per warp):
+//   * the work is the list of 16-token KV blocks of the set's sequences; a fixed grid of CTAs
+//     takes equal, contiguous shares of that list (a share may start or end inside a
+//     sequence), so every CTA streams the same number of bytes and no wave tail is left;
+//   * the warps of a CTA are the KV heads of a head group: warp w walks the CTA's share for KV
+//     head kh = group * warps + w. All warps of a CTA read the same physical blocks at about
+//     the same time, each its head's slice, so every 16 KB block is fetched as a whole;
+//   * a warp streams its blocks itself: lane 0 issues TMA loads (128-byte swizzle, one box per
+//     64-wide half of head_dim and K/V) into the warp's own ring of NSW stages, NSW blocks
+//     ahead of the math; block-table entries come 32 at a time in one coalesced load, one
+//     batch ahead;
+//   * the G = Hq/Hkv query heads of the KV head share every K/V tile: they sit on the M
 //     dimension of the warp-level bf16 MMA (m16n8k16, fp32 accumulate), padded to 16 rows; the
 //     online-softmax state (running max, sum, O) stays in registers; exp2 runs with the scale
 //     folded in;
-//   * a piece that covers its whole unit writes out/lse from registers; a piece cut at a share
-//     edge writes an fp32 partial (normalised O and natural-log LSE), and decode_merge_kernel
-//     folds the pieces of each cut unit with the LSE merge (at most two partial slots per
-//     worker). No shared-memory combine, no block-wide barrier after the prologue.
+//   * a piece that covers its whole sequence writes out/lse from registers; a piece cut at a
+//     share edge writes an fp32 partial (normalised O and natural-log LSE), and
+//     decode_merge_kernel folds the pieces of each cut sequence with the LSE merge (at most
+//     two partial slots per CTA and head). No shared-memory combine, no block-wide barrier
+//     after the prologue.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -32,21 +35,19 @@ namespace pkv {
 
 template <int D>
 struct DecodeCfg {
-  static constexpr int NW = 4;                        // worker warps per CTA
-  static constexpr int NSW = 2;                       // ring stages per worker
+  static constexpr int MAXW = 8;                      // warps (KV heads) per CTA, at most
+  static constexpr int NSW = 2;                       // ring stages per warp
   static constexpr int BS = 16;                       // tokens per block
   static constexpr int HALVES = D / 64;               // 64-element (128-byte) column halves
   static constexpr int TILE_BYTES = BS * D * 2;       // one block of K (or V) for one head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
   static constexpr int Q_BYTES = 16 * D * 2;
-  static constexpr int THREADS = NW * 32;
   static constexpr int MAXR = 1024;     // requests per set handled on device
-  static constexpr int MIN_BLOCKS = 8;  // smallest share (blocks) a worker is given
-  static constexpr int RING_OFF = 0;    // [NW][NSW][K | V]
-  static constexpr int Q_OFF = NW * NSW * STAGE_BYTES;   // [NW][half][16][64]
-  static constexpr int TAB_OFF = Q_OFF + NW * Q_BYTES;   // s_pre[MAXR+1], s_ctx, s_r, s_row
-  static constexpr int BAR_OFF = TAB_OFF + (4 * MAXR + 4) * 4;
-  static constexpr int SMEM = 1024 + BAR_OFF + NW * NSW * 8;
+  static constexpr int MIN_BLOCKS = 8;  // smallest share (blocks) a CTA is given
+  static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;  // s_pre[MAXR+1], s_ctx, s_r, s_row
+  // per-warp region: ring [NSW][K | V], Q [half][16][64], barriers
+  static constexpr int WARP_BYTES = NSW * STAGE_BYTES + Q_BYTES;
+  static constexpr int smem(int nw) { return 1024 + TAB_BYTES + nw * WARP_BYTES + nw * NSW * 8; }
 };
 
 // Resolve the request set: [begin, begin + n) of `order` (or of the identity).
@@ -61,11 +62,11 @@ __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, i
   }
 }
 
-// First block of worker w's share: shares are [w*TB/nw, (w+1)*TB/nw).
+// First block of share w: shares are [w*TB/nw, (w+1)*TB/nw).
 __device__ __forceinline__ int64_t share_start(int w, int64_t TB, int nw) {
   return static_cast<int64_t>(w) * TB / nw;
 }
-// The worker whose share holds block b.
+// The share that holds block b.
 __device__ __forceinline__ int share_of(int64_t b, int64_t TB, int nw) {
   int lo = 0, hi = nw - 1;
   while (lo < hi) {
@@ -74,8 +75,8 @@ __device__ __forceinline__ int share_of(int64_t b, int64_t TB, int nw) {
   }
   return lo;
 }
-// Workers that get work: at least MIN_BLOCKS blocks each.
-__device__ __forceinline__ int active_workers(int64_t TB, int workers, int min_blocks) {
+// Shares that get work: at least MIN_BLOCKS blocks each.
+__device__ __forceinline__ int active_shares(int64_t TB, int workers, int min_blocks) {
   const int64_t want = (TB + min_blocks - 1) / min_blocks;
   return static_cast<int>(want < workers ? (want > 0 ? want : 1) : workers);
 }
@@ -130,17 +131,18 @@ struct PieceIter {
 };
 
 template <int D>
-__global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
+__global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
     const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
   using C = DecodeCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* s_pre = reinterpret_cast<int*>(smem + C::TAB_OFF);
+  const int nthreads = blockDim.x, nw = nthreads >> 5;
+  int* s_pre = reinterpret_cast<int*>(smem + nw * C::WARP_BYTES);
   int* s_ctx = s_pre + C::MAXR + 1;
   int* s_r = s_ctx + C::MAXR;
   int* s_row = s_r + C::MAXR;
-  __shared__ int s_scan[C::THREADS / 32];
+  __shared__ int s_scan[C::MAXW];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.Hkv, G = p.G;
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
   if (n > C::MAXR) n = C::MAXR;
   const int cap = min(p.max_seq_len, p.max_blocks * C::BS);
   int carry = 0;
-  for (int base = 0; base < n; base += C::THREADS) {
+  for (int base = 0; base < n; base += nthreads) {
     const int i = base + tid;
     int cnt = 0;
     if (i < n) {
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
         s_row[i] = 0;
       }
       s_ctx[i] = ctx;
-      cnt = Hkv * ((ctx + C::BS - 1) / C::BS);
+      cnt = (ctx + C::BS - 1) / C::BS;
     }
     int x = cnt;
 #pragma unroll
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
     if (lane == 31) s_scan[warp] = x;
     __syncthreads();
     int wprefix = 0, tot = 0;
-    for (int w = 0; w < C::THREADS / 32; ++w) {
+    for (int w = 0; w < nw; ++w) {
       if (w < warp) wprefix += s_scan[w];
       tot += s_scan[w];
     }
@@ -199,22 +201,23 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
   __syncthreads();
   const int64_t TB = carry;
   if (blockIdx.x == 0) {
-    for (int i = tid; i <= n; i += C::THREADS) p.ws_pre[i] = s_pre[i];
+    for (int i = tid; i <= n; i += nthreads) p.ws_pre[i] = s_pre[i];
   }
   if (TB == 0) return;
 
-  // ---- this warp is worker wk with share [b0, b1) ----
-  const int nwk = active_workers(TB, gridDim.x * C::NW, C::MIN_BLOCKS);
-  const int wk = blockIdx.x * C::NW + warp;
-  if (wk >= nwk) return;  // warp-uniform; nothing below synchronises across warps
-  const int64_t b0 = share_start(wk, TB, nwk), b1 = share_start(wk + 1, TB, nwk);
+  // ---- this CTA's share [b0, b1) of the blocks; this warp's KV head kh ----
+  const int nsh = active_shares(TB, gridDim.x, C::MIN_BLOCKS);
+  const int c = blockIdx.x;
+  const int kh = blockIdx.y * nw + warp;
+  if (c >= nsh || kh >= Hkv) return;  // warp-uniform; nothing below synchronises across warps
+  const int64_t b0 = share_start(c, TB, nsh), b1 = share_start(c + 1, TB, nsh);
   if (b0 >= b1) return;
 
-  uint8_t* ring = smem + C::RING_OFF + warp * C::NSW * C::STAGE_BYTES;
-  uint8_t* sQ = smem + C::Q_OFF + warp * C::Q_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * C::NSW;
+  uint8_t* ring = smem + warp * C::WARP_BYTES;
+  uint8_t* sQ = ring + C::NSW * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + nw * C::WARP_BYTES + C::TAB_BYTES) + warp * C::NSW;
   if (lane == 0) {
-    for (int s = 0; s < C::NSW; ++s) mbar_init(&full[s], 1);
+    for (int st = 0; st < C::NSW; ++st) mbar_init(&full[st], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
 
   // ---- load cursor: walks the share block by block and issues the TMA loads ----
   PieceIter lit;
-  lit.start(s_pre, n, Hkv, b0, b1);
+  lit.start(s_pre, n, 1, b0, b1);
   Piece lpc{0, 0, 0, 0};
   int lj = 0;                 // next block (local index) of lpc to load
   bool lhave = false;         // lpc valid
@@ -261,8 +264,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
       mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_4d(sK + h * 2048, &tm_k, &full[stage], 0, lpc.kh * C::HALVES + h, 0, blk);
-        tma_load_4d(sV + h * 2048, &tm_v, &full[stage], 0, lpc.kh * C::HALVES + h, 0, blk);
+        tma_load_4d(sK + h * 2048, &tm_k, &full[stage], 0, kh * C::HALVES + h, 0, blk);
+        tma_load_4d(sV + h * 2048, &tm_v, &full[stage], 0, kh * C::HALVES + h, 0, blk);
       }
     }
     ++lj;
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
 
   // ---- compute cursor ----
   PieceIter cit;
-  cit.start(s_pre, n, Hkv, b0, b1);
+  cit.start(s_pre, n, 1, b0, b1);
   Piece pc;
   uint32_t t = 0;  // blocks consumed by this worker
   bool ok = true;
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
     for (int c = lane; c < 16 * (D / 8); c += 32) {
       const int gg = c / (D / 8), chunk = c % (D / 8);
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (gg < G) v = *reinterpret_cast<const uint4*>(p.q + (row * p.Hq + pc.kh * G + gg) * D + chunk * 8);
+      if (gg < G) v = *reinterpret_cast<const uint4*>(p.q + (row * p.Hq + kh * G + gg) * D + chunk * 8);
       *reinterpret_cast<uint4*>(sQ + (chunk / 8) * 2048 + sw128(gg, chunk % 8)) = v;
     }
     __syncwarp();
@@ -405,8 +408,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
     }
     const int unit_blocks = (ctx + C::BS - 1) / C::BS;
     const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
-    // partial slot: 0 for a piece that starts this worker's share inside its unit, else 1
-    const int64_t piece_first = s_pre[pc.i] + static_cast<int64_t>(pc.kh) * unit_blocks + pc.lo;
+    // partial slot: 0 for a piece that starts this CTA's share inside its sequence, else 1
+    const int64_t piece_first = s_pre[pc.i] + pc.lo;
     const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -414,7 +417,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
       if (gg >= G) continue;
       const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
       const float lse = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
-      const int hq = pc.kh * G + gg;
+      const int hq = kh * G + gg;
       if (whole) {
         __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + 2 * (lane & 3);
 #pragma unroll
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
           *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
         if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse;
       } else {
-        float* dst = p.ws_part + ((static_cast<int64_t>(wk) * 2 + slot) * G + gg) * (D + 4);
+        float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * Hkv + kh) * G + gg) * (D + 4);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i)
           *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
@@ -436,10 +439,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 2) paged_decode_kernel(
   }
 }
 
-// One warp per (unit, query head): units with no blocks get out = 0, lse = -inf; units cut
-// across worker shares get the LSE merge of their pieces.
+// One warp per (sequence, query head): sequences with no blocks get out = 0, lse = -inf;
+// sequences cut across CTA shares get the LSE merge of their pieces.
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int workers) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int shares) {
   using C = DecodeCfg<D>;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
   const int r = p.order ? p.order[begin + i] : begin + i;
   if (r < 0 || r >= p.batch_reqs) return;
   const int64_t row = p.cu_q ? p.cu_q[r] : r;
-  const int nb = (p.ws_pre[i + 1] - p.ws_pre[i]) / Hkv;
+  const int nb = p.ws_pre[i + 1] - p.ws_pre[i];
   constexpr int PER = D / 32;
   __nv_bfloat16* dst = p.out + (row * p.Hq + h) * D + lane * PER;
   if (nb == 0) {
@@ -463,21 +466,21 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
     return;
   }
   const int64_t TB = p.ws_pre[n];
-  const int nwk = active_workers(TB, workers, C::MIN_BLOCKS);
-  const int64_t first = p.ws_pre[i] + static_cast<int64_t>(kh) * nb;
-  const int w0 = share_of(first, TB, nwk), w1 = share_of(first + nb - 1, TB, nwk);
-  if (w0 == w1) return;  // written whole by the decode kernel
+  const int nsh = active_shares(TB, shares, C::MIN_BLOCKS);
+  const int64_t first = p.ws_pre[i];
+  const int c0 = share_of(first, TB, nsh), c1 = share_of(first + nb - 1, TB, nsh);
+  if (c0 == c1) return;  // written whole by the decode kernel
+  auto part = [&](int c) {
+    return p.ws_part + (((static_cast<int64_t>(c) * 2 + (c == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
+  };
   float M = -CUDART_INF_F;
-  for (int w = w0; w <= w1; ++w) {
-    const float* src = p.ws_part + ((static_cast<int64_t>(w) * 2 + (w == w0 ? 1 : 0)) * G + gg) * (D + 4);
-    M = fmaxf(M, src[D]);
-  }
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, part(c)[D]);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float W = 0.f;
-  for (int w = w0; w <= w1; ++w) {
-    const float* src = p.ws_part + ((static_cast<int64_t>(w) * 2 + (w == w0 ? 1 : 0)) * G + gg) * (D + 4);
+  for (int c = c0; c <= c1; ++c) {
+    const float* src = part(c);
     const float l = src[D];
     const float wt = (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
     W += wt;
@@ -491,36 +494,50 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
   if (p.lse && lane == 0) p.lse[row * p.Hq + h] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
 }
 
-int decode_grid() { return 2 * num_sms(); }
-
-// Partials: [workers][2 slots][G][D + 4] floats (O, then the LSE at index D; rows padded to 16
-// bytes), then the set's block prefix [MAXR + 1] ints for the merge kernel.
-size_t decode_workspace_bytes(int G, int D) {
-  return decode_workspace_pre_offset(G, D) + static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
+// Launch shape: warps per CTA = KV heads per CTA (at most 8); about 8 warps per SM.
+struct DecodeShape {
+  int nw, groups, shares;
+};
+static DecodeShape decode_shape(int Hkv) {
+  DecodeShape d;
+  d.nw = Hkv < DecodeCfg<128>::MAXW ? Hkv : DecodeCfg<128>::MAXW;
+  d.groups = (Hkv + d.nw - 1) / d.nw;
+  const int ctas_per_sm = d.nw >= 8 ? 1 : 8 / d.nw;
+  d.shares = num_sms() * ctas_per_sm / d.groups;
+  if (d.shares < 1) d.shares = 1;
+  return d;
 }
-size_t decode_workspace_pre_offset(int G, int D) {
-  return static_cast<size_t>(decode_grid()) * DecodeCfg<128>::NW * 2 * G * (D + 4) * sizeof(float);
+
+// Partials: [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows padded
+// to 16 bytes), then the set's block prefix [MAXR + 1] ints for the merge kernel.
+size_t decode_workspace_pre_offset(int Hq, int Hkv, int D) {
+  return static_cast<size_t>(decode_shape(Hkv).shares) * 2 * Hq * (D + 4) * sizeof(float);
+}
+size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
+  return decode_workspace_pre_offset(Hq, Hkv, D) + static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
 }
 
 template <int D>
 static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& tk,
                                       const CUtensorMap& tv, cudaStream_t stream, int* launches) {
   using C = DecodeCfg<D>;
-  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D>), C::SMEM,
-                                     D == 64 ? kAttrDecode64 : kAttrDecode128);
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D>),
+                                     C::smem(C::MAXW), D == 64 ? kAttrDecode64 : kAttrDecode128);
   if (e != cudaSuccess) return e;
-  const int grid = decode_grid();
-  paged_decode_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(p, tk, tv);
+  const DecodeShape sh = decode_shape(p.Hkv);
+  paged_decode_kernel<D><<<dim3(sh.shares, sh.groups), sh.nw * 32, C::smem(sh.nw), stream>>>(p, tk, tv);
   *launches += 1;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t warps = static_cast<int64_t>(min(p.max_reqs, C::MAXR)) * p.Hq;
-  decode_merge_kernel<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p, grid * C::NW);
+  decode_merge_kernel<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p, sh.shares);
   *launches += 1;
   return cudaGetLastError();
 }
 
-int decode_smem_bytes(int D) { return D == 64 ? DecodeCfg<64>::SMEM : DecodeCfg<128>::SMEM; }
+int decode_smem_bytes(int D) {
+  return D == 64 ? DecodeCfg<64>::smem(DecodeCfg<64>::MAXW) : DecodeCfg<128>::smem(DecodeCfg<128>::MAXW);
+}
 
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int D, cudaStream_t stream, int* launches) {

@@ -29,7 +29,7 @@ struct DecodeParams {
   int64_t num_blocks;
   int32_t max_seq_len;
   float scale_log2;      // softmax scale * log2(e)
-  float* ws_part;        // [grid][2][G][D + 4] partials of units cut at CTA share edges
+  float* ws_part;        // [shares][2][Hkv][G][D + 4] partials of sequences cut at share edges
   int32_t* ws_pre;       // [set size + 1] block prefix of the set's units (for the merge)
 };
 
@@ -82,9 +82,8 @@ cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* se
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 int D, cudaStream_t stream, int* launches);
 int decode_smem_bytes(int D);
-int decode_grid();
-size_t decode_workspace_bytes(int G, int D);
-size_t decode_workspace_pre_offset(int G, int D);
+size_t decode_workspace_bytes(int Hq, int Hkv, int D);
+size_t decode_workspace_pre_offset(int Hq, int Hkv, int D);
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
 // (ignored for prefill).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -135,6 +135,21 @@ int num_sms() {
   return cache[d];
 }
 
+int max_smem_optin() {
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 227 * 1024;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[d] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess || v <= 0)
+      v = 227 * 1024;
+    cache[d] = v;
+  }
+  return cache[d];
+}
+
 cudaError_t set_smem_attr_once(const void* func, int bytes, int slot) {
   static std::mutex mu;
   static bool done[kAttrCount][kMaxDevices] = {};

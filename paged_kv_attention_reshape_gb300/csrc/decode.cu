@@ -494,6 +494,10 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
   if (p.lse && lane == 0) p.lse[row * p.Hq + h] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
 }
 
+// Largest dynamic shared memory a CTA of this kernel asks for: the device's opt-in limit per
+// block, less room for the kernel's few static shared variables.
+static int max_dyn_smem() { return max_smem_optin() - 1024; }
+
 // Launch shape: warps per CTA = KV heads per CTA (at most 8); about 8 warps per SM.
 struct DecodeShape {
   int nw, groups, shares;
@@ -501,8 +505,12 @@ struct DecodeShape {
 static DecodeShape decode_shape(int Hkv) {
   DecodeShape d;
   d.nw = Hkv < DecodeCfg<128>::MAXW ? Hkv : DecodeCfg<128>::MAXW;
+  while (d.nw > 1 && DecodeCfg<128>::smem(d.nw) > max_dyn_smem()) --d.nw;
   d.groups = (Hkv + d.nw - 1) / d.nw;
-  const int ctas_per_sm = d.nw >= 8 ? 1 : 8 / d.nw;
+  // about 8 warps per SM, as many CTAs as shared memory allows
+  int ctas_per_sm = d.nw >= 8 ? 1 : 8 / d.nw;
+  const int fit = (max_dyn_smem() + 1024) / (DecodeCfg<128>::smem(d.nw) + 1024);
+  if (ctas_per_sm > fit) ctas_per_sm = fit > 0 ? fit : 1;
   d.shares = num_sms() * ctas_per_sm / d.groups;
   if (d.shares < 1) d.shares = 1;
   return d;
@@ -521,8 +529,8 @@ template <int D>
 static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& tk,
                                       const CUtensorMap& tv, cudaStream_t stream, int* launches) {
   using C = DecodeCfg<D>;
-  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D>),
-                                     C::smem(C::MAXW), D == 64 ? kAttrDecode64 : kAttrDecode128);
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D>), max_dyn_smem(),
+                                     D == 64 ? kAttrDecode64 : kAttrDecode128);
   if (e != cudaSuccess) return e;
   const DecodeShape sh = decode_shape(p.Hkv);
   paged_decode_kernel<D><<<dim3(sh.shares, sh.groups), sh.nw * 32, C::smem(sh.nw), stream>>>(p, tk, tv);

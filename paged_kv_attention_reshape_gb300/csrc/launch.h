@@ -68,7 +68,8 @@ enum AttrSlot {
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize once per (kernel slot, device).
 cudaError_t set_smem_attr_once(const void* func, int bytes, int slot);
 
-int num_sms();  // of the current device (cached per device)
+int num_sms();          // of the current device (cached per device)
+int max_smem_optin();   // opt-in shared memory per block of the current device, bytes
 
 cudaError_t launch_kv_cache_write(const void* key, const void* value, const int64_t* slot_mapping,
                                   int64_t num_tokens, const pkv_cache& c, unsigned int* err,

@@ -294,6 +294,8 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   const size_t need = decode_workspace_bytes(p.Hq, p.Hkv, cache.head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   p.ws_part = static_cast<float*>(workspace);
+  p.ws_cut = reinterpret_cast<int4*>(static_cast<char*>(workspace) +
+                                     decode_workspace_cut_offset(p.Hq, p.Hkv, cache.head_dim));
   p.ws_pre = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
                                         decode_workspace_pre_offset(p.Hq, p.Hkv, cache.head_dim));
   CUtensorMap tk, tv;

@@ -62,19 +62,20 @@ __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, i
   }
 }
 
-// First block of share w: shares are [w*TB/nw, (w+1)*TB/nw).
-__device__ __forceinline__ int64_t share_start(int w, int64_t TB, int nw) {
-  return static_cast<int64_t>(w) * TB / nw;
-}
-// The share that holds block b.
-__device__ __forceinline__ int share_of(int64_t b, int64_t TB, int nw) {
-  int lo = 0, hi = nw - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (share_start(mid, TB, nw) <= b) lo = mid; else hi = mid - 1;
+// Balanced partition of TB blocks into nsh shares: share w holds base + (w < rem) blocks.
+struct Shares {
+  int64_t TB, base, rem;
+  int nsh;
+  __device__ Shares(int64_t tb, int n) : TB(tb), base(tb / n), rem(tb % n), nsh(n) {}
+  __device__ int64_t start(int w) const { return w * base + (w < rem ? w : rem); }
+  // the share holding block b
+  __device__ int of(int64_t b) const {
+    const int64_t big = rem * (base + 1);
+    if (b < big) return static_cast<int>(b / (base + 1));
+    return static_cast<int>(rem + (b - big) / base);
   }
-  return lo;
-}
+};
+
 // Shares that get work: at least MIN_BLOCKS blocks each.
 __device__ __forceinline__ int active_shares(int64_t TB, int workers, int min_blocks) {
   const int64_t want = (TB + min_blocks - 1) / min_blocks;
@@ -200,17 +201,27 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   if (tid == 0) s_pre[n] = carry;
   __syncthreads();
   const int64_t TB = carry;
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
     for (int i = tid; i <= n; i += nthreads) p.ws_pre[i] = s_pre[i];
+    // sequences with no context: out = 0, lse = -inf (no share covers them)
+    for (int i = tid; i < n; i += nthreads) {
+      if (s_ctx[i] != 0 || s_r[i] < 0) continue;
+      const int64_t row = s_row[i];
+      uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.Hq * D);
+      for (int c16 = 0; c16 < p.Hq * D / 8; ++c16) dst[c16] = make_uint4(0, 0, 0, 0);
+      if (p.lse)
+        for (int h = 0; h < p.Hq; ++h) p.lse[row * p.Hq + h] = -CUDART_INF_F;
+    }
   }
   if (TB == 0) return;
 
   // ---- this CTA's share [b0, b1) of the blocks; this warp's KV head kh ----
   const int nsh = active_shares(TB, gridDim.x, C::MIN_BLOCKS);
+  const Shares sh(TB, nsh);
   const int c = blockIdx.x;
   const int kh = blockIdx.y * nw + warp;
   if (c >= nsh || kh >= Hkv) return;  // warp-uniform; nothing below synchronises across warps
-  const int64_t b0 = share_start(c, TB, nsh), b1 = share_start(c + 1, TB, nsh);
+  const int64_t b0 = sh.start(c), b1 = sh.start(c + 1);
   if (b0 >= b1) return;
 
   uint8_t* ring = smem + warp * C::WARP_BYTES;
@@ -225,6 +236,16 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   __syncwarp();
 
   // ---- load cursor: walks the share block by block and issues the TMA loads ----
+  // the merge descriptor of boundary c: the sequence cut at b0, if this is the first boundary
+  // inside it, with the shares holding its first and last blocks
+  if (blockIdx.y == 0 && warp == 0 && lane == 0 && c > 0) {
+    PieceIter at;
+    at.start(s_pre, n, 1, b0, b1);
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (at.lo != 0 && sh.of(s_pre[at.i]) == c - 1) d = make_int4(at.i, c - 1, sh.of(s_pre[at.i + 1] - 1), 0);
+    p.ws_cut[c] = d;
+  }
+
   PieceIter lit;
   lit.start(s_pre, n, 1, b0, b1);
   Piece lpc{0, 0, 0, 0};
@@ -439,48 +460,41 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   }
 }
 
-// One warp per (sequence, query head): sequences with no blocks get out = 0, lse = -inf;
-// sequences cut across CTA shares get the LSE merge of their pieces.
+// One CTA per (share boundary c = 1 .. nsh-1, group of four query heads): if the decode kernel
+// recorded that boundary c is the first cut inside a sequence, fold that sequence's pieces
+// (shares c0 .. c1) with the LSE merge, one warp per query head.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int shares) {
   using C = DecodeCfg<D>;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int G = p.G, Hkv = p.Hkv;
-  const int i = static_cast<int>(wid / p.Hq), h = static_cast<int>(wid % p.Hq);
-  const int kh = h / G, gg = h % G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = blockIdx.y * 4 + warp;
+  const int c = blockIdx.x + 1;
+  if (h >= p.Hq) return;
   int begin, n;
   resolve_set(p, begin, n);
   if (n > C::MAXR) n = C::MAXR;
-  if (i >= n) return;
+  if (n == 0) return;
+  const int64_t TB = p.ws_pre[n];
+  if (TB == 0 || c >= active_shares(TB, shares, C::MIN_BLOCKS)) return;  // entry not written
+  const int4 d = p.ws_cut[c];
+  if (d.x < 0) return;
+  const int i = d.x, c0 = d.y, c1 = d.z;
   const int r = p.order ? p.order[begin + i] : begin + i;
   if (r < 0 || r >= p.batch_reqs) return;
   const int64_t row = p.cu_q ? p.cu_q[r] : r;
-  const int nb = p.ws_pre[i + 1] - p.ws_pre[i];
+  const int G = p.G, Hkv = p.Hkv, kh = h / G, gg = h % G;
   constexpr int PER = D / 32;
-  __nv_bfloat16* dst = p.out + (row * p.Hq + h) * D + lane * PER;
-  if (nb == 0) {
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = 0u;
-    if (p.lse && lane == 0) p.lse[row * p.Hq + h] = -CUDART_INF_F;
-    return;
-  }
-  const int64_t TB = p.ws_pre[n];
-  const int nsh = active_shares(TB, shares, C::MIN_BLOCKS);
-  const int64_t first = p.ws_pre[i];
-  const int c0 = share_of(first, TB, nsh), c1 = share_of(first + nb - 1, TB, nsh);
-  if (c0 == c1) return;  // written whole by the decode kernel
-  auto part = [&](int c) {
-    return p.ws_part + (((static_cast<int64_t>(c) * 2 + (c == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
+  auto part = [&](int cc) {
+    return p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
   };
   float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, part(c)[D]);
+  for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, part(cc)[D]);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float W = 0.f;
-  for (int c = c0; c <= c1; ++c) {
-    const float* src = part(c);
+  for (int cc = c0; cc <= c1; ++cc) {
+    const float* src = part(cc);
     const float l = src[D];
     const float wt = (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
     W += wt;
@@ -488,6 +502,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p,
     for (int e = 0; e < PER; ++e) acc[e] += wt * src[lane * PER + e];
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
+  __nv_bfloat16* dst = p.out + (row * p.Hq + h) * D + lane * PER;
 #pragma unroll
   for (int e = 0; e < PER; e += 2)
     *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
@@ -516,10 +531,13 @@ static DecodeShape decode_shape(int Hkv) {
   return d;
 }
 
-// Partials: [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows padded
-// to 16 bytes), then the set's block prefix [MAXR + 1] ints for the merge kernel.
-size_t decode_workspace_pre_offset(int Hq, int Hkv, int D) {
+// Workspace: partials [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows
+// padded to 16 bytes); merge descriptors int4 [shares]; the set's block prefix [MAXR + 1] ints.
+size_t decode_workspace_cut_offset(int Hq, int Hkv, int D) {
   return static_cast<size_t>(decode_shape(Hkv).shares) * 2 * Hq * (D + 4) * sizeof(float);
+}
+size_t decode_workspace_pre_offset(int Hq, int Hkv, int D) {
+  return decode_workspace_cut_offset(Hq, Hkv, D) + static_cast<size_t>(decode_shape(Hkv).shares) * sizeof(int4);
 }
 size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
   return decode_workspace_pre_offset(Hq, Hkv, D) + static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
@@ -537,9 +555,10 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
   *launches += 1;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t warps = static_cast<int64_t>(min(p.max_reqs, C::MAXR)) * p.Hq;
-  decode_merge_kernel<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p, sh.shares);
-  *launches += 1;
+  if (sh.shares > 1) {
+    decode_merge_kernel<D><<<dim3(sh.shares - 1, (p.Hq + 3) / 4), 128, 0, stream>>>(p, sh.shares);
+    *launches += 1;
+  }
   return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@ import time
 
 import numpy as np
 import torch
+import torch.distributed
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -43,6 +44,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device="cpu") -> float:
+    """The largest of every rank's x (the slowest replica sets the job's time); x itself when
+    running alone. `device` is where the process group's backend takes tensors (cuda for
+    NCCL, cpu for gloo)."""
+    if ws <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(units_per_rank: float, ws: int, step_ms: float) -> float:
+    """Whole-job rate of ws replicas that each process units_per_rank per step, timed by the
+    slowest one (step_ms already maxed over ranks): units per second."""
+    return ws * units_per_rank / (step_ms * 1e-3)
 
 
 class Clocks:
@@ -507,17 +525,15 @@ def main():
         w, ms, sec, launches = bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=rank)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
-    step_ms = sum(ms) / len(ms)
-    if ws > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = ws * w["kv_bytes"] / (step_ms * 1e-3) / 1e9
+    step_ms = max_over_ranks(sum(ms) / len(ms), ws, dev)
+    value = replica_rate(w["kv_bytes"], ws, step_ms) / 1e9
     dec_ms = sum(sec["decode"]) / len(sec["decode"])
     achieved = w["alg_bytes"] / (dec_ms * 1e-3) / 1e9
     traffic = profiled_traffic("decode.cu", "paged_decode_qwen3")
+    if ws > 1:
+        torch.distributed.barrier()
     e2e_ms, h2d, d2h = bench_decode_e2e(pkv, w, dev, stream, steps, warmup)
-    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    e2e_step = max_over_ranks(sum(e2e_ms) / len(e2e_ms), ws, dev)
     line = {
         "metric": "paged decode attn KV GB/s (frac of HBM peak); mixed-batch attn tokens/s",
         "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": warmup,
@@ -533,7 +549,7 @@ def main():
                      "traffic": traffic, "algorithmic_bytes_per_launch": w["alg_bytes"],
                      "peak_source": peaks["source"] + " (hbm copy, burst)", "launch_ms": dec_ms},
         "frac_of_nominal_8TBs": w["kv_bytes"] / (dec_ms * 1e-3) / 8e12,
-        "e2e": {"value": ws * w["kv_bytes"] / (e2e_step * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": replica_rate(w["kv_bytes"], ws, e2e_step) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
         "gpu_launches": launches * steps,
         "clocks": clocks.summary(),
@@ -590,7 +606,8 @@ def main():
         torch.cuda.empty_cache()
         line["extras"] = extras
     if rank == 0:
-        line["cpu_baseline"] = oracle_decode_rate(w["b"], budget_s=args.oracle_seconds)
+        if ws == 1:
+            line["cpu_baseline"] = oracle_decode_rate(w["b"], budget_s=args.oracle_seconds)
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()

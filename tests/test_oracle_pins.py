@@ -406,3 +406,24 @@ def test_planted_mistake_is_caught():
     exp = sdpa(qf[0:1], k, v, scale)[0]
     assert np.abs(out[0] - exp).max() < TOL
     assert np.abs(out_w[0] - exp).max() > 1e-3
+
+
+def test_planted_off_by_one_context_is_caught():
+    """An extend oracle that reads one cached key too many (context length off by one), planted
+    here on the CPU by passing seq_len + 1, must fail the masked-SDPA pin."""
+    b = _extend_case(seed=13)
+    scale = 1 / math.sqrt(b.D)
+    args = dict(k_cache=gen.bf16_bits(b.k_cache), v_cache=gen.bf16_bits(b.v_cache),
+                block_tables=b.block_tables.numpy())
+    common = (gen.bf16_bits(b.q), gen.bf16_bits(b.k_new), gen.bf16_bits(b.v_new), b.cu_q.numpy(), scale)
+    r = 2   # 23 new tokens over 50 cached: the table has room for the extra key
+    out, _ = oracle.extend(*common, seq_lens=b.seq_lens.numpy(), **args)
+    out_w, _ = oracle.extend(*common, seq_lens=b.seq_lens.numpy() + 1, **args)
+    qf, kf, vf = (f64(gen.bf16_bits(t)) for t in (b.q, b.k_new, b.v_new))
+    cu = b.cu_q.numpy()
+    s, e = cu[r], cu[r + 1]
+    C = b.seq_lens_list[r] - b.q_lens[r]
+    kc, vc = dense_kv(b, r, C)
+    exp = sdpa(qf[s:e], torch.cat([kc, kf[s:e]]), torch.cat([vc, vf[s:e]]), scale, causal_offset=C)
+    assert np.abs(out[s:e] - exp).max() < TOL
+    assert np.abs(out_w[s:e] - exp).max() > 1e-3

@@ -164,7 +164,9 @@ pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_le
  * sets PKV_DEVERR_LEN and the request is cut to the bound.
  * workspace: device buffer of at least pkv_paged_decode_workspace_size(...) bytes with the
  * same reqs.max_reqs, num_q_heads, head_dim, max_seq_len and cache (it holds the split-KV
- * partials); may be NULL when that size is 0. Calls that share a workspace must not overlap.
+ * partials and their arrival counters); its contents need no initialisation (every call tags
+ * its counters with a value of its own); may be NULL when that size is 0. Calls that share a
+ * workspace must not overlap.
  * ------------------------------------------------------------------------------------- */
 size_t pkv_paged_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim,
@@ -190,7 +192,8 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
  * capture. A call whose scratch need, pkv_paged_decode_workspace_size(...) with the same
  * arguments, exceeds PKV_NOALLOC_SCRATCH_BYTES returns PKV_ERR_WORKSPACE and enqueues
  * nothing. All calls on a device share the one array and it keeps the last call's contents;
- * nothing in it has to start at zero (each call writes every partial it later reads), but
+ * nothing in it has to start at zero (each call writes every partial it later reads and tags
+ * its arrival counters with a value of its own), but
  * calls that overlap on the GPU (other streams, other host threads) race on it: serialise
  * them.
  * ------------------------------------------------------------------------------------- */

@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -53,6 +54,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
   return fn;
+}
+
+// A value per decode call, never 0, so that arrival counters left in a workspace by earlier
+// calls are told apart from this call's.
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> epoch{0};
+  uint32_t e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -294,10 +304,9 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   const size_t need = decode_workspace_bytes(p.Hq, p.Hkv, cache.head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   p.ws_part = static_cast<float*>(workspace);
-  p.ws_cut = reinterpret_cast<int4*>(static_cast<char*>(workspace) +
-                                     decode_workspace_cut_offset(p.Hq, p.Hkv, cache.head_dim));
-  p.ws_pre = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
-                                        decode_workspace_pre_offset(p.Hq, p.Hkv, cache.head_dim));
+  p.ws_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                   decode_workspace_ctr_offset(p.Hq, p.Hkv, cache.head_dim));
+  p.epoch = next_epoch();
   CUtensorMap tk, tv;
   if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
   int launches = 0;

@@ -21,10 +21,14 @@
 //     dimension of the warp-level bf16 MMA (m16n8k16, fp32 accumulate), padded to 16 rows; the
 //     online-softmax state (running max, sum, O) stays in registers; exp2 runs with the scale
 //     folded in;
+//   * the query tile of the next piece is requested (cp.async) when a piece starts, so it is
+//     in shared memory by the time the warp reaches that piece;
 //   * a piece that covers its whole sequence writes out/lse from registers; a piece cut at a
-//     share edge writes an fp32 partial (normalised O and natural-log LSE), and
-//     decode_merge_kernel folds the pieces of each cut sequence with the LSE merge (at most
-//     two partial slots per CTA and head). No shared-memory combine, no block-wide barrier
+//     share edge writes an fp32 partial (normalised O and natural-log LSE, at most two partial
+//     slots per CTA and head) and arrives on a counter of its sequence and KV head; the warp
+//     that arrives last folds the pieces with the LSE merge and writes out/lse. Counters carry
+//     the call's epoch, so a counter left by an earlier call reads as empty and the workspace
+//     needs no clearing. No second kernel, no shared-memory combine, no block-wide barrier
 //     after the prologue.
 #include <math_constants.h>
 
@@ -131,6 +135,168 @@ struct PieceIter {
   }
 };
 
+// Arrival counters of cut sequences hold epoch << 32 | count. A counter whose epoch is not this
+// call's, or whose count is not below the sequence's piece count, was left by an earlier call
+// and counts as empty.
+__device__ __forceinline__ uint32_t arrivals_of(unsigned long long v, uint32_t epoch, int total) {
+  const uint32_t cnt = static_cast<uint32_t>(v);
+  return (static_cast<uint32_t>(v >> 32) != epoch || cnt >= static_cast<uint32_t>(total)) ? 0u : cnt;
+}
+// Count one arrival, starting from `cur`, the counter's value as last read. Returns the
+// arrivals so far, this one included, or 0 if the update kept failing.
+__device__ __forceinline__ int arrive_counter(unsigned long long* ctr, uint32_t epoch, int total,
+                                              unsigned long long cur, unsigned int* err) {
+  for (int it = 0; it < (1 << 16); ++it) {
+    const uint32_t cnt = arrivals_of(cur, epoch, total);
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return static_cast<int>(cnt + 1u);
+    cur = prev;
+  }
+  flag_error(err, PKV_DEVERR_TIMEOUT);
+  return 0;
+}
+
+// The last piece of a cut sequence to finish, with its own result still in registers (the MMA
+// accumulator layout: rows r0 and r0 + 8, columns i*8 + 2*(lane%4) + {0, 1}), folds in the
+// partials of the other pieces (shares c0 .. c1 except `self`) one at a time with the LSE merge
+// (running max, weight sum and sum), and writes out/lse.
+template <int D>
+__device__ __forceinline__ void merge_into_registers(const DecodeParams& p, int64_t row, int kh, int c0,
+                                                     int c1, int self, float (&o)[D / 8][4],
+                                                     const float (&lse_self)[2], const float (&inv_self)[2],
+                                                     int lane) {
+  const int G = p.G, Hkv = p.Hkv, r0 = lane >> 2, col = 2 * (lane & 3);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int gg = r0 + 8 * h;
+    if (gg >= G) continue;
+    float M = lse_self[h], W = lse_self[h] == -CUDART_INF_F ? 0.f : 1.f;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][2 * h] *= inv_self[h];
+      o[i][2 * h + 1] *= inv_self[h];
+    }
+    for (int cc = c0; cc <= c1; ++cc) {
+      if (cc == self) continue;
+      const float* src = p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
+      const float l = __ldcg(src + D);
+      float2 v[D / 8];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) v[i] = __ldcg(reinterpret_cast<const float2*>(src + i * 8 + col));
+      if (l == -CUDART_INF_F) continue;
+      const float m_new = fmaxf(M, l);
+      const float a = __expf(M - m_new), w = __expf(l - m_new);
+      W = W * a + w;
+      M = m_new;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][2 * h] = o[i][2 * h] * a + w * v[i].x;
+        o[i][2 * h + 1] = o[i][2 * h + 1] * a + w * v[i].y;
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const int hq = kh * G + gg;
+    __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + col;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+    if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
+  }
+}
+
+// LSE merge of the partials of one cut sequence, KV head kh, all of them in the workspace (the
+// path of a piece whose arrival, made after it stored its partial, turned out to be the last):
+// the pieces of shares c0 .. c1 (share c0 holds the sequence's first piece in its slot 1; the
+// later shares hold theirs in slot 0, the first piece of their share). One warp. Lane g < G turns query head g's LSEs into
+// weights; then, four heads at a time, every lane loads its elements l*PER .. l*PER+PER-1 of
+// all their pieces before folding them, so each group costs one round trip to L2 (the partials
+// were written by other SMs and are read from L2). A sequence cut into more than MAXP pieces
+// takes several passes, each adding to the fp32 sum the previous one left in the first piece's
+// partial.
+template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeParams& p, int64_t row, int kh, int c0, int c1,
+                                             int lane) {
+  constexpr int PER = D / 32;
+  constexpr int MAXP = 4;  // pieces per pass
+  constexpr int HB = 4;    // heads per group of loads
+  const int G = p.G, Hkv = p.Hkv;
+  const int np = c1 - c0 + 1;
+  auto part = [&](int cc, int gg) {
+    return p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
+  };
+  // lane g: max and sum of weights over all pieces of head g
+  float M = -CUDART_INF_F, W = 0.f;
+  if (lane < G) {
+#pragma unroll 4
+    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldcg(part(cc, lane) + D));
+#pragma unroll 4
+    for (int cc = c0; cc <= c1; ++cc) {
+      const float l = __ldcg(part(cc, lane) + D);
+      W += (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  for (int pb = 0; pb < np; pb += MAXP) {
+    float w[MAXP];
+#pragma unroll
+    for (int k = 0; k < MAXP; ++k) {
+      w[k] = 0.f;
+      if (lane < G && pb + k < np) {
+        const float l = __ldcg(part(c0 + pb + k, lane) + D);
+        w[k] = (l == -CUDART_INF_F) ? 0.f : __expf(l - M) * inv;
+      }
+    }
+    const bool last_pass = pb + MAXP >= np;
+    for (int g0 = 0; g0 < G; g0 += HB) {
+      float v[HB][MAXP + 1][PER];
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb) {
+        const int gg = g0 + hb;
+#pragma unroll
+        for (int k = 0; k <= MAXP; ++k) {
+          // k < MAXP: piece pb + k; k == MAXP: the previous pass's sum
+          const bool use = gg < G && (k < MAXP ? pb + k < np : pb > 0);
+          const float* src = (k < MAXP ? part(c0 + pb + k, gg) : part(c0, gg)) + lane * PER;
+#pragma unroll
+          for (int e = 0; e < PER; e += 2) {
+            float2 x = make_float2(0.f, 0.f);
+            if (use) x = __ldcg(reinterpret_cast<const float2*>(src + e));
+            v[hb][k][e] = x.x;
+            v[hb][k][e + 1] = x.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb) {
+        const int gg = g0 + hb;
+        float acc[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = v[hb][MAXP][e];
+#pragma unroll
+        for (int k = 0; k < MAXP; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w[k], gg & 31);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] += wk * v[hb][k][e];
+        }
+        const float Mg = __shfl_sync(0xffffffffu, M, gg & 31), Wg = __shfl_sync(0xffffffffu, W, gg & 31);
+        if (gg >= G) continue;
+        if (!last_pass) {
+          float* keep = part(c0, gg) + lane * PER;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) __stcg(keep + e, acc[e]);
+        } else {
+          const int hq = kh * G + gg;
+          __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + lane * PER;
+#pragma unroll
+          for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e], acc[e + 1]);
+          if (p.lse && lane == 0) p.lse[row * p.Hq + hq] = Wg > 0.f ? Mg + __logf(Wg) : -CUDART_INF_F;
+        }
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
     const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
@@ -202,7 +368,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   __syncthreads();
   const int64_t TB = carry;
   if (blockIdx.x == 0 && blockIdx.y == 0) {
-    for (int i = tid; i <= n; i += nthreads) p.ws_pre[i] = s_pre[i];
     // sequences with no context: out = 0, lse = -inf (no share covers them)
     for (int i = tid; i < n; i += nthreads) {
       if (s_ctx[i] != 0 || s_r[i] < 0) continue;
@@ -235,40 +400,60 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   }
   __syncwarp();
 
-  // ---- load cursor: walks the share block by block and issues the TMA loads ----
-  // the merge descriptor of boundary c: the sequence cut at b0, if this is the first boundary
-  // inside it, with the shares holding its first and last blocks
-  if (blockIdx.y == 0 && warp == 0 && lane == 0 && c > 0) {
-    PieceIter at;
-    at.start(s_pre, n, 1, b0, b1);
-    int4 d = make_int4(-1, 0, 0, 0);
-    if (at.lo != 0 && sh.of(s_pre[at.i]) == c - 1) d = make_int4(at.i, c - 1, sh.of(s_pre[at.i + 1] - 1), 0);
-    p.ws_cut[c] = d;
+  // ---- query tiles: 16 rows (query heads kh*G .. kh*G+G-1, zero padded) x D, laid out
+  // [half][16][64] with the 128-byte swizzle the ldmatrix addressing expects; requested one
+  // piece ahead with cp.async (rows past G are zero-filled) ----
+  auto request_q = [&](int64_t row) {
+    for (int c16 = lane; c16 < 16 * (D / 8); c16 += 32) {
+      const int gg = c16 / (D / 8), chunk = c16 % (D / 8);
+      const __nv_bfloat16* src = p.q + (row * p.Hq + kh * G + (gg < G ? gg : 0)) * D + chunk * 8;
+      cp_async16(sQ + (chunk / 8) * 2048 + sw128(gg, chunk % 8), src, gg < G ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+
+  PieceIter cit;
+  cit.start(s_pre, n, 1, b0, b1);
+  {
+    PieceIter nx = cit;
+    Piece first;
+    if (nx.next(first)) request_q(s_row[first.i]);
   }
 
+  // ---- load cursor: walks the share block by block and issues the TMA loads ----
   PieceIter lit;
   lit.start(s_pre, n, 1, b0, b1);
   Piece lpc{0, 0, 0, 0};
   int lj = 0;                 // next block (local index) of lpc to load
   bool lhave = false;         // lpc valid
   int lbatch = 0, lnext = 0;  // this lane's table entries: block lpc.lo + lbase + lane (and +32)
+  int lfirst = 0;             // entry `lane` of the piece after lpc, loaded one piece early
   int lbase = 0;
   const int32_t* ltable = nullptr;
   uint32_t issued = 0;        // blocks whose loads were issued
-  auto fetch_entries = [&](int base) {
-    const int nb = lpc.hi - lpc.lo;
-    lbatch = (base + lane < nb) ? ltable[base + lane] : 0;
-    lnext = (base + 32 + lane < nb) ? ltable[base + 32 + lane] : 0;
+  auto table_of = [&](const Piece& q) {
+    return p.block_tables + static_cast<int64_t>(s_r[q.i]) * p.max_blocks + q.lo;
+  };
+  // entry `lane` of the piece after lpc: its load is in flight while lpc streams
+  auto prefetch_following = [&]() {
+    PieceIter nx = lit;
+    Piece q;
+    lfirst = 0;
+    if (nx.next(q) && lane < q.hi - q.lo) lfirst = table_of(q)[lane];
   };
   // Issue the next block of the share into `stage`; false when the share is exhausted.
   auto issue_next = [&](int stage) -> bool {
     if (!lhave || lj == lpc.hi - lpc.lo) {
+      const bool first = !lhave;
       if (!lit.next(lpc)) return false;
       lhave = true;
       lj = 0;
       lbase = 0;
-      ltable = p.block_tables + static_cast<int64_t>(s_r[lpc.i]) * p.max_blocks + lpc.lo;
-      fetch_entries(0);
+      ltable = table_of(lpc);
+      const int nb = lpc.hi - lpc.lo;
+      lbatch = first ? ((lane < nb) ? ltable[lane] : 0) : lfirst;
+      lnext = (32 + lane < nb) ? ltable[32 + lane] : 0;
+      prefetch_following();
     } else if (lj == lbase + 32) {
       lbase += 32;
       lbatch = lnext;
@@ -298,23 +483,46 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   for (int s = 0; s < C::NSW; ++s)
     if (more) more = issue_next(s);
 
+  // ---- deferred arrival of the last stored partial ----
+  bool pend = false;
+  unsigned long long* pend_ctr = nullptr;
+  unsigned long long pend_cur = 0;  // lane 0: the counter as read when the piece ended
+  int pend_np = 0, pend_c0 = 0, pend_c1 = 0;
+  int64_t pend_row = 0;
+  // merges this warp owes after its arrivals completed a count (at most one per stored
+  // partial, so at most two per share); run once the share is done
+  int due = 0;
+  int due_c0[2] = {0, 0}, due_c1[2] = {0, 0};
+  int64_t due_row[2] = {0, 0};
+  auto flush_arrival = [&]() {
+    __threadfence();
+    __syncwarp();
+    int arrived = 0;
+    if (lane == 0) arrived = arrive_counter(pend_ctr, p.epoch, pend_np, pend_cur, p.err);
+    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+    pend = false;
+    if (arrived == pend_np) {
+      if (due < 2) {
+        due_c0[due] = pend_c0;
+        due_c1[due] = pend_c1;
+        due_row[due] = pend_row;
+        ++due;
+      } else if (lane == 0) {
+        flag_error(p.err, PKV_DEVERR_REQS);  // cannot happen: a share stores at most two partials
+      }
+    }
+  };
+
   // ---- compute cursor ----
-  PieceIter cit;
-  cit.start(s_pre, n, 1, b0, b1);
   Piece pc;
   uint32_t t = 0;  // blocks consumed by this worker
   bool ok = true;
   const int r0 = lane >> 2;  // fragment rows r0 and r0 + 8
   while (ok && cit.next(pc)) {
-    // Q tile of the piece: 16 rows (query heads kh*G .. kh*G+G-1, zero padded) x D, laid out
-    // [half][16][64] with the 128-byte swizzle the ldmatrix addressing expects
+    // the piece's query tile (requested one piece earlier) into A fragments, then request the
+    // next piece's tile into the same buffer
     const int64_t row = s_row[pc.i];
-    for (int c = lane; c < 16 * (D / 8); c += 32) {
-      const int gg = c / (D / 8), chunk = c % (D / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (gg < G) v = *reinterpret_cast<const uint4*>(p.q + (row * p.Hq + kh * G + gg) * D + chunk * 8);
-      *reinterpret_cast<uint4*>(sQ + (chunk / 8) * 2048 + sw128(gg, chunk % 8)) = v;
-    }
+    cp_async_wait_all();
     __syncwarp();
     uint32_t qa[D / 16][4];
     {
@@ -323,6 +531,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       for (int ks = 0; ks < D / 16; ++ks)
         ldsm_x4(qbase + (ks / 4) * 2048 + sw128(lane & 15, (ks % 4) * 2 + (lane >> 4)), qa[ks][0], qa[ks][1],
                 qa[ks][2], qa[ks][3]);
+    }
+    __syncwarp();
+    {
+      PieceIter nx = cit;
+      Piece np;
+      if (nx.next(np)) request_q(s_row[np.i]);
     }
     const int ctx = s_ctx[pc.i];
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows r0 and r0 + 8 (log2 units)
@@ -419,6 +633,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       fence_proxy_async_smem();
       __syncwarp();
       if (more) more = issue_next(s);
+      if (pend) flush_arrival();
     }
     if (!ok) break;
     // ---- the piece's result ----
@@ -432,81 +647,71 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
     // partial slot: 0 for a piece that starts this CTA's share inside its sequence, else 1
     const int64_t piece_first = s_pre[pc.i] + pc.lo;
     const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
+    float inv[2], lse[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+      lse[h] = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+    if (whole) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gg = r0 + 8 * h;
+        if (gg >= G) continue;
+        const int hq = kh * G + gg;
+        __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + 2 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+          *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+        if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse[h];
+      }
+      continue;
+    }
+    // A cut piece. Its sequence's pieces are those of shares c0 .. c1. A piece that ends this
+    // share first looks whether all the others have arrived: then it is the last and merges
+    // them into its registers, storing nothing of its own. Otherwise it stores its partial
+    // and arrives on the counter after the next block (its stores have completed by then), so
+    // the arrival costs the stream little; the arrival that completes the count merges.
+    const int c0 = sh.of(s_pre[pc.i]), c1 = sh.of(s_pre[pc.i + 1] - 1), npc = c1 - c0 + 1;
+    unsigned long long* ctr = p.ws_ctr + static_cast<int64_t>(c0) * Hkv + kh;
+    unsigned long long cur = 0;
+    if (lane == 0) cur = atomicAdd(ctr, 0ull);
+    if (slot == 1) {
+      const int prior = __shfl_sync(0xffffffffu, static_cast<int>(arrivals_of(cur, p.epoch, npc)), 0);
+      if (prior == npc - 1) {
+        __threadfence();
+        merge_into_registers<D>(p, row, kh, c0, c1, c, o, lse, inv, lane);
+        continue;
+      }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int gg = r0 + 8 * h;
       if (gg >= G) continue;
-      const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
-      const float lse = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
-      const int hq = kh * G + gg;
-      if (whole) {
-        __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + 2 * (lane & 3);
+      float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * Hkv + kh) * G + gg) * (D + 4);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-          *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
-        if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse;
-      } else {
-        float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * Hkv + kh) * G + gg) * (D + 4);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-          *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
-        if ((lane & 3) == 0) dst[D] = lse;
-      }
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+      if ((lane & 3) == 0) dst[D] = lse[h];
     }
+    pend = true;
+    pend_ctr = ctr;
+    pend_cur = cur;
+    pend_np = npc;
+    pend_c0 = c0;
+    pend_c1 = c1;
+    pend_row = row;
+  }
+  if (ok && pend) flush_arrival();
+  if (ok && due > 0) {
+    __threadfence();
+    for (int k = 0; k < due; ++k) merge_pieces<D>(p, due_row[k], kh, due_c0[k], due_c1[k], lane);
   }
   // after a timeout, wait (bounded) for this worker's loads still in flight before exiting
   for (; t < issued; ++t) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[t % C::NSW], (t / C::NSW) & 1, p.err))) break;
   }
-}
-
-// One CTA per (share boundary c = 1 .. nsh-1, group of four query heads): if the decode kernel
-// recorded that boundary c is the first cut inside a sequence, fold that sequence's pieces
-// (shares c0 .. c1) with the LSE merge, one warp per query head.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p, int shares) {
-  using C = DecodeCfg<D>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int h = blockIdx.y * 4 + warp;
-  const int c = blockIdx.x + 1;
-  if (h >= p.Hq) return;
-  int begin, n;
-  resolve_set(p, begin, n);
-  if (n > C::MAXR) n = C::MAXR;
-  if (n == 0) return;
-  const int64_t TB = p.ws_pre[n];
-  if (TB == 0 || c >= active_shares(TB, shares, C::MIN_BLOCKS)) return;  // entry not written
-  const int4 d = p.ws_cut[c];
-  if (d.x < 0) return;
-  const int i = d.x, c0 = d.y, c1 = d.z;
-  const int r = p.order ? p.order[begin + i] : begin + i;
-  if (r < 0 || r >= p.batch_reqs) return;
-  const int64_t row = p.cu_q ? p.cu_q[r] : r;
-  const int G = p.G, Hkv = p.Hkv, kh = h / G, gg = h % G;
-  constexpr int PER = D / 32;
-  auto part = [&](int cc) {
-    return p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * Hkv + kh) * G + gg) * (D + 4);
-  };
-  float M = -CUDART_INF_F;
-  for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, part(cc)[D]);
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float W = 0.f;
-  for (int cc = c0; cc <= c1; ++cc) {
-    const float* src = part(cc);
-    const float l = src[D];
-    const float wt = (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
-    W += wt;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += wt * src[lane * PER + e];
-  }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  __nv_bfloat16* dst = p.out + (row * p.Hq + h) * D + lane * PER;
-#pragma unroll
-  for (int e = 0; e < PER; e += 2)
-    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
-  if (p.lse && lane == 0) p.lse[row * p.Hq + h] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
+  cp_async_wait_all();
 }
 
 // Largest dynamic shared memory a CTA of this kernel asks for: the device's opt-in limit per
@@ -532,15 +737,13 @@ static DecodeShape decode_shape(int Hkv) {
 }
 
 // Workspace: partials [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows
-// padded to 16 bytes); merge descriptors int4 [shares]; the set's block prefix [MAXR + 1] ints.
-size_t decode_workspace_cut_offset(int Hq, int Hkv, int D) {
+// padded to 16 bytes), then the arrival counters [shares][Hkv] of cut sequences (8 bytes each).
+size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D) {
   return static_cast<size_t>(decode_shape(Hkv).shares) * 2 * Hq * (D + 4) * sizeof(float);
 }
-size_t decode_workspace_pre_offset(int Hq, int Hkv, int D) {
-  return decode_workspace_cut_offset(Hq, Hkv, D) + static_cast<size_t>(decode_shape(Hkv).shares) * sizeof(int4);
-}
 size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
-  return decode_workspace_pre_offset(Hq, Hkv, D) + static_cast<size_t>(DecodeCfg<128>::MAXR + 1) * sizeof(int);
+  return decode_workspace_ctr_offset(Hq, Hkv, D) +
+         static_cast<size_t>(decode_shape(Hkv).shares) * Hkv * sizeof(unsigned long long);
 }
 
 template <int D>
@@ -553,12 +756,6 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
   const DecodeShape sh = decode_shape(p.Hkv);
   paged_decode_kernel<D><<<dim3(sh.shares, sh.groups), sh.nw * 32, C::smem(sh.nw), stream>>>(p, tk, tv);
   *launches += 1;
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (sh.shares > 1) {
-    decode_merge_kernel<D><<<dim3(sh.shares - 1, (p.Hq + 3) / 4), 128, 0, stream>>>(p, sh.shares);
-    *launches += 1;
-  }
   return cudaGetLastError();
 }
 

@@ -30,8 +30,8 @@ struct DecodeParams {
   int32_t max_seq_len;
   float scale_log2;      // softmax scale * log2(e)
   float* ws_part;        // [shares][2][Hkv][G][D + 4] partials of sequences cut at share edges
-  int4* ws_cut;          // [shares] merge descriptors {sequence, first share, last share}
-  int32_t* ws_pre;       // [set size + 1] block prefix of the set's sequences (for the merge)
+  unsigned long long* ws_ctr;  // [shares][Hkv] arrival counters of cut sequences: epoch << 32 | count
+  uint32_t epoch;        // distinct per call: counters left by earlier calls read as empty
 };
 
 // Extend and prefill share one kernel; prefill is the case without cached context.
@@ -85,8 +85,7 @@ cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, co
                                 int D, cudaStream_t stream, int* launches);
 int decode_smem_bytes(int D);
 size_t decode_workspace_bytes(int Hq, int Hkv, int D);
-size_t decode_workspace_pre_offset(int Hq, int Hkv, int D);
-size_t decode_workspace_cut_offset(int Hq, int Hkv, int D);
+size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D);
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
 // (ignored for prefill).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

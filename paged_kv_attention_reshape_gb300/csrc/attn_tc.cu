@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
   __shared__ int s_abort;
   __shared__ int s_scan[12];
 
+  pdl_wait();
+  pdl_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   int begin, n;
@@ -515,9 +517,10 @@ static cudaError_t launch_attention_tc_impl(const AttnParams& p, const CUtensorM
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&attention_tc_kernel<D>), C::SMEM,
                                      D == 64 ? kAttrAttn64 : kAttrAttn128);
   if (e != cudaSuccess) return e;
-  attention_tc_kernel<D><<<num_sms(), C::THREADS, C::SMEM, stream>>>(p, tq, tk, tv, tck, tcv);
+  e = launch_pdl(attention_tc_kernel<D>, dim3(num_sms()), dim3(C::THREADS), C::SMEM, stream, p, tq, tk, tv,
+                 tck, tcv);
   *launches += 1;
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -22,6 +22,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+// Every kernel of the library is launched so that it may start while the previous kernel on
+// the stream finishes (launch_pdl). Its first act is pdl_wait: it returns once the grids it
+// depends on have completed and their memory is visible, so stream order holds for every byte
+// the kernel touches; only the launch latency overlaps. pdl_release then lets the next grid
+// begin its own launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier -----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

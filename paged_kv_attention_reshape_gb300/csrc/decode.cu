@@ -311,6 +311,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
   int* s_row = s_r + C::MAXR;
   __shared__ int s_scan[C::MAXW];
 
+  pdl_wait();
+  pdl_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.Hkv, G = p.G;
 
@@ -754,9 +756,10 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
                                      D == 64 ? kAttrDecode64 : kAttrDecode128);
   if (e != cudaSuccess) return e;
   const DecodeShape sh = decode_shape(p.Hkv);
-  paged_decode_kernel<D><<<dim3(sh.shares, sh.groups), sh.nw * 32, C::smem(sh.nw), stream>>>(p, tk, tv);
+  e = launch_pdl(paged_decode_kernel<D>, dim3(sh.shares, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
+                 p, tk, tv);
   *launches += 1;
-  return cudaGetLastError();
+  return e;
 }
 
 int decode_smem_bytes(int D) {

@@ -7,6 +7,7 @@
 // Both are HBM-bound byte copies: 16-byte vector loads and stores, many in flight per thread,
 // streaming cache hints (the data is touched once).
 #include "common.cuh"
+#include "launch.h"
 
 namespace pkv {
 
@@ -29,6 +30,8 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int64_t num_slots, int32_t block_size, int64_t block_stride_chunks,
     int32_t row_chunks, unsigned int* err) {
+  pdl_wait();
+  pdl_release();
   const int lane = threadIdx.x & 31;
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= num_tokens) return;
@@ -68,6 +71,8 @@ __global__ void __launch_bounds__(256) kv_block_pack_kernel(
     const uint4* __restrict__ k_cache, const uint4* __restrict__ v_cache,
     const int32_t* __restrict__ block_ids, int32_t num_ids, int64_t num_blocks,
     int64_t block_stride_chunks, int64_t block_chunks, uint4* __restrict__ dst, unsigned int* err) {
+  pdl_wait();
+  pdl_release();
   const int32_t i = blockIdx.x;
   const int which = blockIdx.y;
   const int64_t b = block_ids[i];
@@ -99,11 +104,10 @@ cudaError_t launch_kv_cache_write(const void* key, const void* value, const int6
   const int32_t row_chunks = c.num_kv_heads * c.head_dim * 2 / 16;
   const int64_t threads = num_tokens * 32;
   const int64_t blocks = (threads + 255) / 256;
-  kv_cache_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), slot_mapping, num_tokens,
-      static_cast<uint4*>(c.k), static_cast<uint4*>(c.v), c.num_blocks * c.block_size,
-      c.block_size, c.stride_block * 2 / 16, row_chunks, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_cache_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value), slot_mapping, num_tokens,
+                    static_cast<uint4*>(c.k), static_cast<uint4*>(c.v), c.num_blocks * c.block_size,
+                    c.block_size, c.stride_block * 2 / 16, row_chunks, err);
 }
 
 cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, int32_t num_ids,
@@ -111,10 +115,9 @@ cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, i
   const int64_t block_chunks =
       static_cast<int64_t>(c.block_size) * c.num_kv_heads * c.head_dim * 2 / 16;
   dim3 grid(num_ids, 2);
-  kv_block_pack_kernel<<<grid, 256, 0, stream>>>(
-      static_cast<const uint4*>(c.k), static_cast<const uint4*>(c.v), block_ids, num_ids,
-      c.num_blocks, c.stride_block * 2 / 16, block_chunks, static_cast<uint4*>(dst), err);
-  return cudaGetLastError();
+  return launch_pdl(kv_block_pack_kernel, grid, dim3(256), 0, stream, static_cast<const uint4*>(c.k),
+                    static_cast<const uint4*>(c.v), block_ids, num_ids, c.num_blocks, c.stride_block * 2 / 16,
+                    block_chunks, static_cast<uint4*>(dst), err);
 }
 
 }  // namespace pkv

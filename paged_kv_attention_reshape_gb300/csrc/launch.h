@@ -57,6 +57,24 @@ struct AttnParams {
   float scale_log2;
 };
 
+// Launch with programmatic stream serialisation: the kernel may begin launching while the
+// previous kernel on the stream runs; it waits (pdl_wait) before touching memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Indices into the per-device "dynamic shared memory attribute set" table.
 enum AttrSlot {
   kAttrDecode64 = 0,

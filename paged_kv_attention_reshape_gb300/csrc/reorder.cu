@@ -6,9 +6,11 @@
 // One CTA of 1024 threads walks the requests in chunks of 1024: every thread classifies one
 // request, warp ballots give each request its rank among the earlier requests of its class in
 // the chunk, and a running per-class offset carries over chunks, so the order within a class
-// is the arrival order (a stable partition). A second pass writes the reordered query starts;
+// is the arrival order (a stable partition). A batch of one chunk reads its lengths once and
+// keeps them in registers and shared memory for all passes. A second pass writes the reordered query starts;
 // an optional grid kernel maps reordered token positions to arrival positions by binary search.
 #include "common.cuh"
+#include "launch.h"
 
 namespace pkv {
 
@@ -30,15 +32,30 @@ __global__ void __launch_bounds__(kReorderThreads) batch_classify_reorder_kernel
   __shared__ int s_total[3];
   __shared__ int s_base[3];
   __shared__ int s_scan[kReorderWarps];
+  __shared__ int s_len[kReorderThreads];  // one chunk: query lengths in reordered order
+  pdl_wait();
+  pdl_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
+  // A batch of at most one chunk keeps each request's class and length in its thread's
+  // registers from the first read on; larger batches read them again in every pass.
+  const bool one_chunk = R <= kReorderThreads;
+  int my_cls = -1, my_len = 0;
+  if (one_chunk && tid < R) {
+    my_len = cu_q[tid + 1] - cu_q[tid];
+    my_cls = my_len <= threshold ? PKV_CLASS_DECODE : (seq_lens[tid] > my_len ? PKV_CLASS_EXTEND : PKV_CLASS_PREFILL);
+  }
 
   // pass 1: class totals
   if (tid < 3) s_total[tid] = 0;
   __syncthreads();
   {
     int cnt[3] = {0, 0, 0};
-    for (int r = tid; r < R; r += kReorderThreads) cnt[classify(cu_q, seq_lens, r, threshold)]++;
+    if (one_chunk) {
+      if (my_cls >= 0) cnt[my_cls]++;
+    } else {
+      for (int r = tid; r < R; r += kReorderThreads) cnt[classify(cu_q, seq_lens, r, threshold)]++;
+    }
 #pragma unroll
     for (int c = 0; c < 3; ++c) {
       int v = cnt[c];
@@ -62,7 +79,7 @@ __global__ void __launch_bounds__(kReorderThreads) batch_classify_reorder_kernel
   // pass 2: stable positions, chunk by chunk
   for (int base = 0; base < R; base += kReorderThreads) {
     const int r = base + tid;
-    const int cls = r < R ? classify(cu_q, seq_lens, r, threshold) : -1;
+    const int cls = one_chunk ? my_cls : (r < R ? classify(cu_q, seq_lens, r, threshold) : -1);
     unsigned m[3];
 #pragma unroll
     for (int c = 0; c < 3; ++c) m[c] = __ballot_sync(0xffffffffu, cls == c);
@@ -76,6 +93,7 @@ __global__ void __launch_bounds__(kReorderThreads) batch_classify_reorder_kernel
       for (int w = 0; w < warp; ++w) before += s_warp_cnt[cls][w];
       const int pos = s_base[cls] + before + __popc(m[cls] & lt_mask);
       perm[pos] = r;
+      if (one_chunk) s_len[pos] = my_len;
     }
     __syncthreads();
     if (tid < 3) {
@@ -96,8 +114,12 @@ __global__ void __launch_bounds__(kReorderThreads) batch_classify_reorder_kernel
     const int j = base + tid;
     int v = 0;
     if (j < R) {
-      const int r = perm[j];
-      v = cu_q[r + 1] - cu_q[r];
+      if (one_chunk) {
+        v = s_len[j];
+      } else {
+        const int r = perm[j];
+        v = cu_q[r + 1] - cu_q[r];
+      }
     }
     int x = v;
 #pragma unroll
@@ -130,6 +152,8 @@ __global__ void __launch_bounds__(256) token_map_kernel(const int32_t* __restric
                                                         const int32_t* __restrict__ cu_r,
                                                         int32_t R, int64_t T,
                                                         int32_t* __restrict__ token_map) {
+  pdl_wait();
+  pdl_release();
   const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (p >= T) return;
   // last j with cu_r[j] <= p (requests with no tokens are skipped naturally)
@@ -151,17 +175,15 @@ cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* se
                                           int64_t num_tokens, cudaStream_t stream,
                                           int* launches) {
   int32_t* cu_r = cu_q_reordered;  // the host requires it whenever token_map is requested
-  batch_classify_reorder_kernel<<<1, kReorderThreads, 0, stream>>>(cu_q, seq_lens, R, threshold,
-                                                                   perm, bounds, cu_r);
+  cudaError_t e = launch_pdl(batch_classify_reorder_kernel, dim3(1), dim3(kReorderThreads), 0, stream, cu_q,
+                             seq_lens, R, threshold, perm, bounds, cu_r);
   *launches += 1;
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (token_map && num_tokens > 0 && R > 0) {
     const int64_t blocks = (num_tokens + 255) / 256;
-    token_map_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(cu_q, perm, cu_r, R,
-                                                                       num_tokens, token_map);
+    e = launch_pdl(token_map_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, cu_q,
+                   static_cast<const int32_t*>(perm), static_cast<const int32_t*>(cu_r), R, num_tokens, token_map);
     *launches += 1;
-    e = cudaGetLastError();
   }
   return e;
 }

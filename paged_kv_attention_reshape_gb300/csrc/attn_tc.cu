@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "softmax.cuh"
 #include "tc.cuh"
 
 namespace pkv {
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
           tc::wait_ld();
           if (full) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+            for (int e = 0; e < 32; e += 2) mx = sm::max3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -279,24 +280,49 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         // pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs over the first half of S
         const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
         float rs = 0.f;
+        if (full) {
+          // every column valid: pairs of columns in packed fp32 (one instruction per pair for
+          // the scale-and-shift and the running sum)
+          const uint64_t sc2 = sm::f2(p.scale_log2, p.scale_log2), nm2 = sm::f2(neg_m, neg_m);
+          uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tc::ld32(srow + c * 32, v);
-          tc::wait_ld();
-          uint32_t pk[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tc::ld32(srow + c * 32, v);
+            tc::wait_ld();
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, neg_m));
-            if (!full) {
+            for (int e = 0; e < 32; e += 2) {
+              const uint64_t x = sm::fma2(sm::f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+              float x0, x1;
+              sm::unf2(x, x0, x1);
+              const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
+              rs2 = sm::add2(rs2, pp);
+              pk[e / 2] = sm::bf16x2(pp);
+            }
+            tc::st16(srow + c * 16, pk);
+          }
+          float r0, r1;
+          sm::unf2(rs2, r0, r1);
+          rs = r0 + r1;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tc::ld32(srow + c * 32, v);
+            tc::wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2, neg_m));
+              float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, neg_m));
               p0 = (c * 32 + e < kv) ? p0 : 0.f;
               p1 = (c * 32 + e + 1 < kv) ? p1 : 0.f;
+              rs += p0 + p1;
+              pk[e / 2] = pack_bf16(p0, p1);
             }
-            rs += p0 + p1;
-            pk[e / 2] = pack_bf16(p0, p1);
+            tc::st16(srow + c * 16, pk);
           }
-          tc::st16(srow + c * 16, pk);
         }
         l = l * alpha + rs;
         // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole

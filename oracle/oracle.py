@@ -51,6 +51,8 @@ def _load():
             lib.oracle_kv_cache_write.restype = i64
             lib.oracle_kv_block_pack.argtypes = [P, P, i64, i64, P, i32, P]
             lib.oracle_kv_block_pack.restype = i32
+            lib.oracle_kv_block_unpack.argtypes = [P, P, i32, P, P, i64, i64]
+            lib.oracle_kv_block_unpack.restype = i32
             lib.oracle_batch_classify_reorder.argtypes = [P, P, i32, i32, P, P, P, P]
             lib.oracle_batch_classify_reorder.restype = None
             lib.oracle_lse_merge.argtypes = [P, P, P, P, i64, i32, P, P]
@@ -117,6 +119,22 @@ def kv_block_pack(k_cache, v_cache, block_ids, dst=None):
     bad = lib.oracle_kv_block_pack(_ptr(k_cache), _ptr(v_cache), nb, block_elems,
                                    _ptr(block_ids), n, _ptr(dst))
     return dst, int(bad)
+
+
+def kv_block_unpack(src, block_ids, k_cache, v_cache):
+    """Scatter packed blocks src [2, n, bs, Hkv, D] into the caches in place (uint16 bits);
+    returns the count of ids outside the pool."""
+    lib = _load()
+    src = _c(src, np.uint16)
+    block_ids = _c(block_ids, np.int32)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+    nb = k_cache.shape[0]
+    block_elems = int(np.prod(k_cache.shape[1:]))
+    n = block_ids.shape[0]
+    assert src.shape[0] == 2 and src.shape[1] == n and int(np.prod(src.shape[2:])) == block_elems
+    return int(lib.oracle_kv_block_unpack(_ptr(src), _ptr(block_ids), n, _ptr(k_cache), _ptr(v_cache),
+                                          nb, block_elems))
 
 
 def batch_classify_reorder(cu_q, seq_lens, threshold=1):

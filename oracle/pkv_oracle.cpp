@@ -194,6 +194,30 @@ int32_t oracle_kv_block_pack(const uint16_t* k_cache, const uint16_t* v_cache, i
   return bad;
 }
 
+// ---- kv_block_unpack ----------------------------------------------------------------------
+// [MORI-IO] "Read mode vs write mode": the decode instance receives each layer's KV into the
+// blocks it allocated for the request. The receiving side of a staged transfer: src holds the
+// layer's blocks as kv_block_pack lays them out ([2][n][block_elems], K blocks then V blocks)
+// and block i lands in cache block block_ids[i]. Ids outside [0, num_blocks) are skipped and
+// counted (the return value); with repeated ids the later entry wins.
+int32_t oracle_kv_block_unpack(const uint16_t* src, const int32_t* block_ids, int32_t n,
+                               uint16_t* k_cache, uint16_t* v_cache, int64_t num_blocks,
+                               int64_t block_elems) {
+  int32_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t b = block_ids[i];
+    if (b < 0 || b >= num_blocks) {
+      ++bad;
+      continue;
+    }
+    for (int64_t e = 0; e < block_elems; ++e) {
+      k_cache[b * block_elems + e] = src[static_cast<int64_t>(i) * block_elems + e];
+      v_cache[b * block_elems + e] = src[(static_cast<int64_t>(n) + i) * block_elems + e];
+    }
+  }
+  return bad;
+}
+
 // ---- batch_classify_reorder -------------------------------------------------------------
 // [ROCm-attn] "key innovations", batch reorder: requests are put in [decode:extend:prefill]
 // order with reorder_batch_threshold = 1. Class: decode if q_len <= threshold, else extend if

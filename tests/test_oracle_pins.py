@@ -122,6 +122,42 @@ def test_pack_flags_bad_ids():
     assert np.array_equal(dst[0, 0], kc[3]) and np.array_equal(dst[0, 3], kc[0])
 
 
+def test_unpack_matches_numpy_assignment_and_inverts_pack():
+    """MORI-IO "Read mode vs write mode": the receiving instance lands each layer's blocks in
+    the ids it allocated. unpack == numpy fancy-index assignment; pack then unpack into a
+    second pool moves exactly the listed blocks and nothing else."""
+    rng = np.random.default_rng(11)
+    nb, n = 40, 13
+    kc = rng.integers(0, 1 << 16, size=(nb, 16, 2, 8), dtype=np.uint16)
+    vc = rng.integers(0, 1 << 16, size=(nb, 16, 2, 8), dtype=np.uint16)
+    src_ids = rng.permutation(nb)[:n].astype(np.int32)
+    dst_ids = rng.permutation(nb)[:n].astype(np.int32)
+    packed, bad = oracle.kv_block_pack(kc, vc, src_ids)
+    assert bad == 0
+    k2 = rng.integers(0, 1 << 16, size=kc.shape, dtype=np.uint16)
+    v2 = rng.integers(0, 1 << 16, size=vc.shape, dtype=np.uint16)
+    ek, ev = k2.copy(), v2.copy()
+    ek[dst_ids] = kc[src_ids]
+    ev[dst_ids] = vc[src_ids]
+    assert oracle.kv_block_unpack(packed, dst_ids, k2, v2) == 0
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+    # the round trip onto the same ids restores the listed blocks of the source pool
+    k3, v3 = np.zeros_like(kc), np.zeros_like(vc)
+    oracle.kv_block_unpack(packed, src_ids, k3, v3)
+    assert np.array_equal(k3[src_ids], kc[src_ids]) and np.array_equal(v3[src_ids], vc[src_ids])
+    others = np.setdiff1d(np.arange(nb), src_ids)
+    assert not k3[others].any() and not v3[others].any()
+
+
+def test_unpack_skips_and_counts_bad_ids():
+    src = np.arange(2 * 3 * 16 * 8, dtype=np.uint16).reshape(2, 3, 16, 1, 8)
+    kc = np.zeros((4, 16, 1, 8), np.uint16)
+    vc = np.zeros_like(kc)
+    assert oracle.kv_block_unpack(src, np.array([2, 7, -3], np.int32), kc, vc) == 2
+    assert np.array_equal(kc[2], src[0, 0]) and np.array_equal(vc[2], src[1, 0])
+    assert kc.sum() == src[0, 0].sum()
+
+
 # ---- reorder -----------------------------------------------------------------------------------
 
 def _classify_brute(q_lens, seq_lens, thr):

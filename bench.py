@@ -388,13 +388,23 @@ def bench_attention_only(pkv, dev, stream, timer, steps, warmup, kind):
 
 
 def bench_write_pack(pkv, dev, stream, timer, steps, warmup):
+    """80 layers: write each layer's prompt K/V into its cache, pack each layer's blocks into
+    its own staging buffer, and land each staging buffer in its own receiving pool at shuffled
+    block ids. Every launch touches buffers of its own, so no layer's data is still in L2
+    when a later launch reads it (the 80 layers hold about 16 GB)."""
     layers = gen.write_pack_layers(**gen.WRITE_PACK_LLAMA70B, device=dev)
     L0 = layers[0]
     nblk = L0.block_ids.numel()
-    dst = torch.empty((2, nblk) + tuple(L0.k_cache.shape[1:]), dtype=torch.bfloat16, device=dev)
+    shape = (2, nblk) + tuple(L0.k_cache.shape[1:])
+    dsts = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in layers]
+    g = torch.Generator().manual_seed(10)
+    recv_nb = L0.k_cache.shape[0]
+    recv = [(torch.empty_like(L0.k_cache), torch.empty_like(L0.v_cache),
+             torch.randperm(recv_nb, generator=g)[:nblk].to(torch.int32).to(dev)) for _ in layers]
     row_bytes = L0.key.numel() * 2
     write_bytes = len(layers) * (2 * row_bytes * 2 + L0.slot_mapping.numel() * 8)   # read + write, K and V
-    pack_bytes = len(layers) * (2 * dst.numel() * 2 // 1 + nblk * 4)   # read + write
+    pack_bytes = len(layers) * (2 * dsts[0].numel() * 2 + nblk * 4)   # read + write
+    unpack_bytes = pack_bytes
 
     def step(marks):
         def w():
@@ -402,14 +412,19 @@ def bench_write_pack(pkv, dev, stream, timer, steps, warmup):
                 pkv.kv_cache_write(L.key, L.value, L.slot_mapping, L.k_cache, L.v_cache, stream=stream)
 
         def p():
-            for L in layers:
-                pkv.kv_block_pack(L.k_cache, L.v_cache, L.block_ids, dst=dst, stream=stream)
+            for L, d in zip(layers, dsts):
+                pkv.kv_block_pack(L.k_cache, L.v_cache, L.block_ids, dst=d, stream=stream)
+
+        def u():
+            for d, (rk, rv, ids) in zip(dsts, recv):
+                pkv.kv_block_unpack(d, ids, rk, rv, stream=stream)
         mark(marks, "write", stream, w)
         mark(marks, "pack", stream, p)
+        mark(marks, "unpack", stream, u)
 
     ms, sec = timer.run(step, steps, warmup)
-    del layers
-    return dict(ms=ms, sec=sec, write_bytes=write_bytes, pack_bytes=pack_bytes)
+    del layers, dsts, recv
+    return dict(ms=ms, sec=sec, write_bytes=write_bytes, pack_bytes=pack_bytes, unpack_bytes=unpack_bytes)
 
 
 # ---- CPU oracle ---------------------------------------------------------------------------------
@@ -614,12 +629,16 @@ def main():
             r = bench_write_pack(pkv, dev, stream, timer, max(3, steps // 2), warmup)
             tw = sum(r["sec"]["write"]) / len(r["sec"]["write"])
             tp = sum(r["sec"]["pack"]) / len(r["sec"]["pack"])
-            extras["write_pack"] = {"workload": "80 layers x 10000 tokens, Hkv 8, D 128 (320 KiB/token)",
+            tu = sum(r["sec"]["unpack"]) / len(r["sec"]["unpack"])
+            extras["write_pack"] = {"workload": "80 layers x 10000 tokens, Hkv 8, D 128 (320 KiB/token); "
+                                                "each layer packed, then landed in a receiving pool",
                                     "write_gbs": r["write_bytes"] / (tw * 1e-3) / 1e9,
                                     "pack_gbs": r["pack_bytes"] / (tp * 1e-3) / 1e9,
                                     "write_ms_80_layers": tw, "pack_ms_80_layers": tp,
                                     "write_frac": r["write_bytes"] / (tw * 1e-3) / 1e9 / peaks["hbm"],
-                                    "pack_frac": r["pack_bytes"] / (tp * 1e-3) / 1e9 / peaks["hbm"]}
+                                    "pack_frac": r["pack_bytes"] / (tp * 1e-3) / 1e9 / peaks["hbm"],
+                                    "unpack_gbs": r["unpack_bytes"] / (tu * 1e-3) / 1e9, "unpack_ms_80_layers": tu,
+                                    "unpack_frac": r["unpack_bytes"] / (tu * 1e-3) / 1e9 / peaks["hbm"]}
         except Exception as e:
             extras["write_pack"] = {"error": repr(e)}
         torch.cuda.empty_cache()

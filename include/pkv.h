@@ -261,6 +261,21 @@ pkv_status pkv_kv_block_pack(pkv_cache cache, const int32_t* block_ids, int32_t 
                              void* dst, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * kv_block_unpack — land one layer's packed KV blocks in a cache's block ids (the receiving
+ * side of the per-layer handoff that kv_block_pack stages).
+ * Source: vLLM blog "moriio-kv-connector", section "Read mode vs write mode" (the decode
+ * instance receives each layer's KV into the blocks it allocated for the request; the
+ * transfer is described by block size and per-layer stride).
+ * src (bf16, 16-byte aligned) = [2][num_ids][block_size][num_kv_heads][head_dim], as
+ * kv_block_pack writes it: cache.k block block_ids[i] = src[0][i], cache.v block
+ * block_ids[i] = src[1][i]. An id outside [0, num_blocks) is skipped and sets
+ * PKV_DEVERR_BLOCK. Ids are expected to be distinct; with a repeated id, which of its copies
+ * lands is unspecified. src must not overlap the cache.
+ * ------------------------------------------------------------------------------------- */
+pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
+                               pkv_cache cache, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * pkv_device_errors — read (and, if clear != 0, reset) the error word of the current device.
  * Synchronises `stream` first. *flags (host) receives an OR of PKV_DEVERR_* bits. Returns
  * PKV_ERR_DEVICE when the word was non-zero, PKV_OK otherwise.

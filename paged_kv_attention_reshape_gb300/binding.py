@@ -103,6 +103,18 @@ def kv_block_pack(k_cache, v_cache, block_ids, dst=None, stream=None):
     return dst
 
 
+def kv_block_unpack(src, block_ids, k_cache, v_cache, stream=None):
+    """k_cache[block_ids[i]] = src[0][i], v_cache[block_ids[i]] = src[1][i] (in place)."""
+    lib = _lib.load()
+    _need(src, torch.bfloat16, "src")
+    _need(block_ids, torch.int32, "block_ids")
+    cache = make_cache(k_cache, v_cache)
+    n = block_ids.numel()
+    if tuple(src.shape) != (2, n) + tuple(k_cache.shape[1:]):
+        raise ValueError(f"src shape {tuple(src.shape)} does not match 2 x {n} blocks of {tuple(k_cache.shape[1:])}")
+    _check(lib.pkv_kv_block_unpack(_ptr(src), _ptr(block_ids), n, cache, _stream(stream)), "kv_block_unpack")
+
+
 def batch_classify_reorder(cu_q, seq_lens, decode_threshold=1, perm=None, bounds=None,
                            cu_q_reordered=None, token_map=None, with_token_map=False,
                            num_tokens=None, stream=None):

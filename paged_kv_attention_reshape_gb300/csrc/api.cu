@@ -240,6 +240,22 @@ pkv_status pkv_kv_block_pack(pkv_cache cache, const int32_t* block_ids, int32_t 
   return st;
 }
 
+pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
+                               pkv_cache cache, pkv_stream_t stream) {
+  if (num_ids < 0) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if (num_ids == 0) return PKV_OK;
+  if (block_ids == nullptr || src == nullptr || !aligned16(src)) return PKV_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * 2) % 16 != 0)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_ids > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
+  st = cuda_status(launch_kv_block_unpack(src, block_ids, num_ids, cache, error_word(),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+  t_launches += 1;
+  return st;
+}
+
 pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens,
                                       int32_t num_reqs, int32_t decode_threshold, int32_t* perm,
                                       int32_t* bounds, int32_t* cu_q_reordered, int32_t* token_map,

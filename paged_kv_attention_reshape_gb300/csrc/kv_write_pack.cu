@@ -3,7 +3,9 @@
 //     "rocm-attention-backend", "Unified attention backends": stage 1 of every forward writes
 //     the new K/V into the cache);
 //   kv_block_pack: gather one layer's blocks by id into a contiguous staging buffer (vLLM blog
-//     "moriio-kv-connector", "Write mode": the prefill instance pushes each layer's KV blocks).
+//     "moriio-kv-connector", "Write mode": the prefill instance pushes each layer's KV blocks);
+//   kv_block_unpack: land such a buffer in the receiving pool's block ids (same blog, "Read
+//     mode vs write mode": the decode instance receives into the blocks it allocated).
 // Both are HBM-bound byte copies: 16-byte vector loads and stores, many in flight per thread,
 // streaming cache hints (the data is touched once).
 #include "common.cuh"
@@ -98,6 +100,38 @@ __global__ void __launch_bounds__(256) kv_block_pack_kernel(
   }
 }
 
+// blockIdx.y selects K (0) or V (1); blockIdx.x is the source block index i.
+__global__ void __launch_bounds__(256) kv_block_unpack_kernel(
+    const uint4* __restrict__ src, const int32_t* __restrict__ block_ids, int32_t num_ids, int64_t num_blocks,
+    int64_t block_stride_chunks, int64_t block_chunks, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+    unsigned int* err) {
+  pdl_wait();
+  pdl_release();
+  const int32_t i = blockIdx.x;
+  const int which = blockIdx.y;
+  const int64_t b = block_ids[i];
+  if (b < 0 || b >= num_blocks) {
+    if (threadIdx.x == 0 && which == 0) flag_error(err, PKV_DEVERR_BLOCK);
+    return;
+  }
+  const uint4* in = src + (static_cast<int64_t>(which) * num_ids + i) * block_chunks;
+  uint4* out = (which == 0 ? k_cache : v_cache) + b * block_stride_chunks;
+  constexpr int U = 8;
+  for (int64_t c0 = threadIdx.x; c0 < block_chunks; c0 += static_cast<int64_t>(blockDim.x) * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + static_cast<int64_t>(u) * blockDim.x;
+      if (c < block_chunks) v[u] = ld_stream(in + c);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + static_cast<int64_t>(u) * blockDim.x;
+      if (c < block_chunks) out[c] = v[u];
+    }
+  }
+}
+
 cudaError_t launch_kv_cache_write(const void* key, const void* value, const int64_t* slot_mapping,
                                   int64_t num_tokens, const pkv_cache& c, unsigned int* err,
                                   cudaStream_t stream) {
@@ -118,6 +152,16 @@ cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, i
   return launch_pdl(kv_block_pack_kernel, grid, dim3(256), 0, stream, static_cast<const uint4*>(c.k),
                     static_cast<const uint4*>(c.v), block_ids, num_ids, c.num_blocks, c.stride_block * 2 / 16,
                     block_chunks, static_cast<uint4*>(dst), err);
+}
+
+cudaError_t launch_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
+                                   const pkv_cache& c, unsigned int* err, cudaStream_t stream) {
+  const int64_t block_chunks =
+      static_cast<int64_t>(c.block_size) * c.num_kv_heads * c.head_dim * 2 / 16;
+  dim3 grid(num_ids, 2);
+  return launch_pdl(kv_block_unpack_kernel, grid, dim3(256), 0, stream, static_cast<const uint4*>(src), block_ids,
+                    num_ids, c.num_blocks, c.stride_block * 2 / 16, block_chunks, static_cast<uint4*>(c.k),
+                    static_cast<uint4*>(c.v), err);
 }
 
 }  // namespace pkv

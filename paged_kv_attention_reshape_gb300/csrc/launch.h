@@ -95,6 +95,8 @@ cudaError_t launch_kv_cache_write(const void* key, const void* value, const int6
                                   cudaStream_t stream);
 cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, int32_t num_ids,
                                  void* dst, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
+                                   const pkv_cache& c, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens, int32_t R,
                                           int32_t threshold, int32_t* perm, int32_t* bounds,
                                           int32_t* cu_q_reordered, int32_t* token_map,

@@ -74,6 +74,10 @@ def test_host_checks_reject_bad_arguments_without_a_gpu(lib):
                                1.0, fake, None, None, 0, None) == 2
     assert lib.pkv_varlen_prefill_attn(fake, fake, fake, 8, fake, reqs, 64, 2, 128, 8, 1.0, fake,
                                        None, None) == 2
+    # unpack: misaligned source, negative count, empty
+    assert lib.pkv_kv_block_unpack(P((1 << 20) + 4), fake, 3, cache, None) == 1
+    assert lib.pkv_kv_block_unpack(fake, fake, -1, cache, None) == 1
+    assert lib.pkv_kv_block_unpack(None, None, 0, cache, None) == 0
     # token map without reordered starts
     assert lib.pkv_batch_classify_reorder(fake, fake, 4, 1, fake, fake, None, fake, 10, None) == 1
     # identity set larger than the batch

@@ -146,8 +146,8 @@ def test_prefill_4x8k_full(pkv):
 
 def test_write_pack_llama70b_full(pkv):
     """80 layers x 10000 tokens, Hkv 8, D 128 (320 KiB/token): all 80 layers written and packed as
-    in the benchmark; 8 sampled layers compared bit for bit (caches and packed buffers), and a
-    shuffled-order pack of one layer."""
+    in the benchmark; 8 sampled layers compared bit for bit (caches and packed buffers), a
+    shuffled-order pack of one layer, and its unpack into another pool."""
     layers = gen.write_pack_layers(**gen.WRITE_PACK_LLAMA70B, device="cuda")
     sample = set(np.random.default_rng(4).choice(len(layers), 8, replace=False).tolist())
     before = {i: (_host(L.k_cache).copy(), _host(L.v_cache).copy()) for i, L in enumerate(layers) if i in sample}
@@ -173,3 +173,15 @@ def test_write_pack_llama70b_full(pkv):
     dst = pkv.kv_block_pack(L.k_cache, L.v_cache, shuf)
     exp, _ = oracle.kv_block_pack(_host(L.k_cache), _host(L.v_cache), shuf.cpu().numpy())
     assert np.array_equal(_host(dst), exp)
+    # the receiving side: land the packed layer in another pool's blocks (as the benchmark's
+    # handoff does), bit for bit the oracle's
+    g = torch.Generator().manual_seed(10)
+    recv_k = gen.randn_bf16(tuple(L.k_cache.shape), g, "cpu")
+    recv_v = gen.randn_bf16(tuple(L.v_cache.shape), g, "cpu")
+    recv_ids = torch.randperm(L.k_cache.shape[0], generator=g)[:shuf.numel()].to(torch.int32)
+    rk, rv = recv_k.to(L.k_cache.device), recv_v.to(L.k_cache.device)
+    pkv.kv_block_unpack(dst, recv_ids.to(L.k_cache.device), rk, rv)
+    assert pkv.device_errors() == 0
+    ek, ev = _host(recv_k).copy(), _host(recv_v).copy()
+    assert oracle.kv_block_unpack(exp, recv_ids.numpy(), ek, ev) == 0
+    assert np.array_equal(_host(rk), ek) and np.array_equal(_host(rv), ev)

@@ -95,6 +95,43 @@ def test_kv_block_pack_duplicates_and_bad_ids(pkv):
     assert _errors(pkv) & 0x2
 
 
+# ---- kv_block_unpack -------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Hkv,D", [(8, 128), (2, 64), (1, 8)])
+def test_kv_block_unpack_bit_exact(pkv, Hkv, D):
+    """Pack from one pool, unpack into another at different ids: bit for bit the oracle's."""
+    g = torch.Generator().manual_seed(21 + Hkv)
+    nb, n = 300, 97
+    src_k, src_v = gen.randn_bf16((nb, 16, Hkv, D), g, "cpu"), gen.randn_bf16((nb, 16, Hkv, D), g, "cpu")
+    dst_k, dst_v = gen.randn_bf16((nb, 16, Hkv, D), g, "cpu"), gen.randn_bf16((nb, 16, Hkv, D), g, "cpu")
+    src_ids = torch.randperm(nb, generator=g)[:n].to(torch.int32)
+    dst_ids = torch.randperm(nb, generator=g)[:n].to(torch.int32)
+    gk, gv = dst_k.to(DEV), dst_v.to(DEV)
+    packed = pkv.kv_block_pack(src_k.to(DEV), src_v.to(DEV), src_ids.to(DEV))
+    pkv.kv_block_unpack(packed, dst_ids.to(DEV), gk, gv)
+    exp_packed, _ = oracle.kv_block_pack(bits(src_k), bits(src_v), src_ids.numpy())
+    ek, ev = bits(dst_k).copy(), bits(dst_v).copy()
+    assert oracle.kv_block_unpack(exp_packed, dst_ids.numpy(), ek, ev) == 0
+    assert np.array_equal(bits(gk), ek) and np.array_equal(bits(gv), ev)
+    assert _errors(pkv) == 0
+
+
+def test_kv_block_unpack_strided_cache_and_bad_ids(pkv):
+    """Caches that are slices of a wider pool (block stride > block), and ids outside the
+    pool: skipped, flagged, the rest landed."""
+    g = torch.Generator().manual_seed(5)
+    pool = gen.randn_bf16((10, 2, 16, 2, 64), g, "cpu")       # [blocks][K|V][16][Hkv][D]
+    src = gen.randn_bf16((2, 4, 16, 2, 64), g, "cpu")
+    ids = torch.tensor([3, 11, -1, 7], dtype=torch.int32)
+    gpool = pool.to(DEV)
+    gk, gv = gpool[:, 0], gpool[:, 1]
+    pkv.kv_block_unpack(src.to(DEV), ids.to(DEV), gk, gv)
+    ek, ev = bits(pool[:, 0]).copy(), bits(pool[:, 1]).copy()
+    assert oracle.kv_block_unpack(bits(src), ids.numpy(), ek, ev) == 2
+    assert np.array_equal(bits(gk.contiguous()), ek) and np.array_equal(bits(gv.contiguous()), ev)
+    assert _errors(pkv) & 0x2
+
+
 # ---- batch_classify_reorder ------------------------------------------------------------------
 
 def _reorder_case(R, seed, thr=1):

@@ -60,6 +60,16 @@ def _load():
             lib.oracle_paged_decode.argtypes = [P, P, P, i64, i32, i32, i32, P, i32, P, P, P,
                                                 i32, i32, f64, P, P, i32]
             lib.oracle_paged_decode.restype = None
+            f32 = ctypes.c_float
+            lib.oracle_e4m3_decode.argtypes = [P, i64, P]
+            lib.oracle_e4m3_decode.restype = None
+            lib.oracle_e4m3_encode.argtypes = [P, i64, P]
+            lib.oracle_e4m3_encode.restype = None
+            lib.oracle_kv_cache_write_fp8.argtypes = [P, P, P, i64, i32, i32, i32, i64, f32, f32, P, P]
+            lib.oracle_kv_cache_write_fp8.restype = i64
+            lib.oracle_paged_decode_fp8.argtypes = [P, P, P, i64, i32, i32, i32, P, i32, P, P, P,
+                                                    i32, i32, f64, f64, f64, P, P, i32]
+            lib.oracle_paged_decode_fp8.restype = None
             lib.oracle_extend.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, P, i32, i32,
                                           i32, i32, f64, P, P, P, i32]
             lib.oracle_extend.restype = None
@@ -135,6 +145,61 @@ def kv_block_unpack(src, block_ids, k_cache, v_cache):
     assert src.shape[0] == 2 and src.shape[1] == n and int(np.prod(src.shape[2:])) == block_elems
     return int(lib.oracle_kv_block_unpack(_ptr(src), _ptr(block_ids), n, _ptr(k_cache), _ptr(v_cache),
                                           nb, block_elems))
+
+
+def e4m3_decode(codes):
+    """float64 values of E4M3 codes (uint8)."""
+    lib = _load()
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    lib.oracle_e4m3_decode(_ptr(codes), codes.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x):
+    """E4M3 codes (round to nearest even, saturating at +-448) of float32 values."""
+    lib = _load()
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib.oracle_e4m3_encode(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def kv_cache_write_fp8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    """Quantise bf16 rows (bits) into E4M3 caches (uint8, in place); returns bad-slot count."""
+    lib = _load()
+    key, value = _c(key, np.uint16), _c(value, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    T, hkv, D = key.shape
+    nb, bs = k_cache.shape[:2]
+    return int(lib.oracle_kv_cache_write_fp8(_ptr(key), _ptr(value), _ptr(slot_mapping), T, hkv, D, bs, nb,
+                                             float(k_scale), float(v_scale), _ptr(k_cache), _ptr(v_cache)))
+
+
+def paged_decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale, v_scale, cu_q=None,
+                     req_ids=None, n_req=None, nthreads=None, out=None, lse=None):
+    """paged_decode over E4M3 caches (uint8 codes [nb, bs, Hkv, D]) with per-tensor scales."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    k_cache, v_cache = _c(k_cache, np.uint8), _c(v_cache, np.uint8)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    cu_q, req_ids = _c(cu_q, np.int32), _c(req_ids, np.int32)
+    T, Hq, D = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    assert d2 == D and Hq % hkv == 0
+    if n_req is None:
+        n_req = req_ids.shape[0] if req_ids is not None else seq_lens.shape[0]
+    if out is None:
+        out = np.full((T, Hq, D), np.nan)
+    if lse is None:
+        lse = np.full((T, Hq), np.nan)
+    lib.oracle_paged_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, D, _ptr(block_tables),
+                                block_tables.shape[1], _ptr(seq_lens), _ptr(cu_q), _ptr(req_ids), n_req, Hq,
+                                float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
+                                nthreads or default_threads())
+    return out, lse
 
 
 def batch_classify_reorder(cu_q, seq_lens, threshold=1):

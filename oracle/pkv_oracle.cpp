@@ -112,6 +112,40 @@ void attend_row(const double* q, const double* keys, const double* vals, int64_t
   *lse = m + std::log(z);
 }
 
+// ---- OCP 8-bit floating point E4M3 ("E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+// bits, no infinities; exponent field 0 encodes subnormals m * 2^-9; S.1111.111 is NaN, so the
+// largest finite magnitude is 1.75 * 2^8 = 448.
+inline double e4m3_value(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+  double v;
+  if ((c & 0x7F) == 0x7F)
+    v = std::numeric_limits<double>::quiet_NaN();
+  else if (e == 0)
+    v = std::ldexp(static_cast<double>(m), -9);
+  else
+    v = std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+// Round to the nearest E4M3 value, ties to the even code (even mantissa), with magnitudes above
+// 448 saturating to 448 (the "satfinite" conversion). Plain search over the 127 finite
+// magnitudes, in double, from the float's exact value.
+inline uint8_t e4m3_encode(float x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(x));
+  if (a >= 448.0) return sign | 0x7E;
+  int best = 0;
+  double best_err = a;  // code 0 = +0
+  for (int c = 1; c < 0x7F; ++c) {
+    const double err = std::fabs(e4m3_value(static_cast<uint8_t>(c)) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return sign | static_cast<uint8_t>(best);
+}
+
 struct Paged {
   const uint16_t* k_cache;
   const uint16_t* v_cache;
@@ -427,6 +461,78 @@ void oracle_extend_chunked(const uint16_t* q, const uint16_t* k_new, const uint1
       }
     }
   }
+}
+
+// ---- FP8 (E4M3) KV cache ---------------------------------------------------------------
+// [ROCm-attn] MLA section: the cached context can be dequantised while it is gathered
+// ("gather_and_maybe_dequant_cache"); the pages' models are served in FP8. A cache of E4M3
+// codes with one scale per tensor: code c stands for e4m3(c) * scale. Writing a bf16 row
+// stores e4m3_encode(float(x) * (1.0f / scale)), the product and the reciprocal taken in
+// float, as a kernel computes them.
+void oracle_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+void oracle_e4m3_encode(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+
+int64_t oracle_kv_cache_write_fp8(const uint16_t* key, const uint16_t* value, const int64_t* slot_mapping,
+                                  int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int64_t num_blocks, float k_scale, float v_scale,
+                                  uint8_t* k_cache, uint8_t* v_cache) {
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  const int64_t nslots = num_blocks * block_size;
+  const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+  int64_t bad = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    if (s >= nslots) {
+      ++bad;
+      continue;
+    }
+    const int64_t dst = ((s / block_size) * block_size + s % block_size) * row;
+    for (int64_t e = 0; e < row; ++e) {
+      const float kx = static_cast<float>(bf16_value(key[t * row + e]));
+      const float vx = static_cast<float>(bf16_value(value[t * row + e]));
+      k_cache[dst + e] = e4m3_encode(kx * k_inv);
+      v_cache[dst + e] = e4m3_encode(vx * v_inv);
+    }
+  }
+  return bad;
+}
+
+// Decode against an E4M3 cache: oracle_paged_decode with every cached key and value
+// dequantised (code value times the tensor's scale) before the same fp64 attention.
+void oracle_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                             int64_t num_blocks, int32_t bs, int32_t Hkv, int32_t D,
+                             const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                             const int32_t* cu_q, const int32_t* req_ids, int32_t n_req, int32_t Hq,
+                             double scale, double k_scale, double v_scale, double* out, double* lse,
+                             int32_t nthreads) {
+  const Paged P{nullptr, nullptr, num_blocks, bs, Hkv, D, block_tables, max_blocks};
+  const int G = Hq / Hkv;
+  parallel_for(static_cast<int64_t>(n_req) * Hkv, nthreads, [&](int64_t item) {
+    const int64_t r = req_ids ? req_ids[item / Hkv] : item / Hkv;
+    const int kh = static_cast<int>(item % Hkv);
+    const int64_t row = cu_q ? cu_q[r] : r;
+    const int64_t n = seq_lens[r];
+    std::vector<double> K(static_cast<size_t>(std::max<int64_t>(n, 0)) * D),
+        V(static_cast<size_t>(std::max<int64_t>(n, 0)) * D), qd(D);
+    for (int64_t j = 0; j < n; ++j) {
+      const int64_t off = paged_offset(P, r, j, kh);
+      for (int d = 0; d < D; ++d) {
+        K[j * D + d] = off < 0 ? NAN : e4m3_value(k_cache[off + d]) * k_scale;
+        V[j * D + d] = off < 0 ? NAN : e4m3_value(v_cache[off + d]) * v_scale;
+      }
+    }
+    for (int g = 0; g < G; ++g) {
+      const int h = kh * G + g;
+      for (int d = 0; d < D; ++d) qd[d] = bf16_value(q[(row * Hq + h) * D + d]);
+      attend_row(qd.data(), K.data(), V.data(), n, D, scale, out + (row * Hq + h) * D,
+                 lse + row * Hq + h);
+    }
+  });
 }
 
 }  // extern "C"

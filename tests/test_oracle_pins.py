@@ -463,3 +463,79 @@ def test_planted_off_by_one_context_is_caught():
     exp = sdpa(qf[s:e], torch.cat([kc, kf[s:e]]), torch.cat([vc, vf[s:e]]), scale, causal_offset=C)
     assert np.abs(out[s:e] - exp).max() < TOL
     assert np.abs(out_w[s:e] - exp).max() > 1e-3
+
+
+# ---- FP8 (E4M3) KV cache -------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch_float8():
+    """All 256 codes against torch's float8_e4m3fn (an independent implementation of the OCP
+    E4M3 format): equal values, NaN at the same codes, largest finite 448, smallest subnormal
+    2^-9."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.nanmax(ours) == 448.0 and ours[1] == 2.0 ** -9
+
+
+def test_e4m3_encode_rounds_to_nearest_even_and_saturates():
+    """Round to nearest, ties to even, against torch's conversion on values below 464 (torch
+    turns larger ones into NaN); above that, the saturating definition: +-448."""
+    rng = np.random.default_rng(31)
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))          # the 127 finite magnitudes
+    mids = (grid[1:] + grid[:-1]) / 2                                   # exact ties
+    x = np.concatenate([rng.normal(0, 8, 20000), rng.uniform(-463, 463, 20000), mids, -mids,
+                        grid, rng.uniform(0, 2 ** -6, 2000)]).astype(np.float32)
+    ours = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    big = np.array([464, 470, 1e6, 3.4e38, -500, -1e30], np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E] * 4 + [0xFE] * 2
+
+
+def test_fp8_write_matches_numpy_quantise_and_scatter():
+    """code = E4M3(float(x) * float(1 / scale)) scattered through the slot mapping."""
+    layers = gen.write_pack_layers(1, 100, Hkv=2, D=16, seed=33)
+    L = layers[0]
+    nb = L.k_cache.shape[0]
+    kc = np.zeros((nb, 16, 2, 16), np.uint8)
+    vc = np.zeros_like(kc)
+    ks, vs = 0.037, 0.011
+    assert oracle.kv_cache_write_fp8(gen.bf16_bits(L.key), gen.bf16_bits(L.value), L.slot_mapping.numpy(),
+                                     kc, vc, ks, vs) == 0
+    def quant(t, s):
+        inv = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(s, dtype=torch.float32)
+        return (t.float() * inv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    slots = L.slot_mapping.numpy()
+    ek, ev = np.zeros_like(kc), np.zeros_like(vc)
+    ek.reshape(-1, 2, 16)[slots] = quant(L.key, ks)
+    ev.reshape(-1, 2, 16)[slots] = quant(L.value, vs)
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def test_fp8_decode_matches_torch_sdpa_on_dequantised_cache():
+    """Decode over an E4M3 cache == fp64 SDPA over the dequantised keys/values (codes through
+    torch's float8 decoding, times the scales)."""
+    b = gen.decode_batch(3, 5, 60, Hq=8, Hkv=2, D=16, seed=34)
+    rng = np.random.default_rng(35)
+    kc = rng.integers(0, 256, size=tuple(b.k_cache.shape), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=tuple(b.v_cache.shape), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x11                                      # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x22
+    ks, vs, scale = 0.02, 0.5, 0.25
+    out, lse = oracle.paged_decode_fp8(gen.bf16_bits(b.q), kc, vc, b.block_tables.numpy(),
+                                       b.seq_lens.numpy(), scale, ks, vs)
+    deq = lambda c, s: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64) * s
+    kd, vd = deq(kc, ks).numpy(), deq(vc, vs).numpy()
+    qf = f64(gen.bf16_bits(b.q))
+    for r in range(b.R):
+        n = b.seq_lens_list[r]
+        pos = np.arange(n)
+        blk = b.block_tables.numpy()[r, pos // 16]
+        k = torch.from_numpy(kd[blk, pos % 16])
+        v = torch.from_numpy(vd[blk, pos % 16])
+        exp = sdpa(qf[r:r + 1], k, v, scale)[0]
+        assert np.abs(out[r] - exp).max() < TOL
+        assert np.abs(lse[r] - lse_ref(qf[r:r + 1], k, scale)[0]).max() < TOL

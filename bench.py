@@ -260,6 +260,38 @@ def bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=0):
     return w, ms, {"decode": launch_ms}, launches
 
 
+def bench_decode_fp8(pkv, dev, stream, timer, steps, warmup):
+    """The headline step over an FP8 (E4M3) cache: same batch, caches holding codes (synthesised
+    from the bf16 values with per-tensor scales), new tokens quantised by kv_cache_write."""
+    w = decode_workload(pkv, dev)
+    b, meta, R = w["b"], w["meta"], w["b"].R
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    del b.k_cache, b.v_cache
+    torch.cuda.empty_cache()
+    kv_bytes = sum(b.seq_lens_list) * b.Hkv * b.D * 2
+    other = b.q.numel() * 2 * 2 + R * b.Hq * 4 + sum((x + 15) // 16 for x in b.seq_lens_list) * 4
+    reqs = pkv.Reqs(max_reqs=R, batch_reqs=R, order=w["perm"], bounds=w["bounds"], cls=pkv.CLASS_DECODE)
+    scale = 1.0 / math.sqrt(b.D)
+
+    def decode():
+        pkv.paged_decode_attn(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], w["maxs"], cu_q=meta["cu_q"],
+                              reqs=reqs, scale=scale, out=w["out"], lse=w["lse"], workspace=w["ws"], stream=stream,
+                              k_scale=ks, v_scale=vs)
+
+    def step(marks):
+        pkv.batch_classify_reorder(meta["cu_q"], meta["seq_lens"], perm=w["perm"], bounds=w["bounds"],
+                                   cu_q_reordered=w["cu_r"], stream=stream)
+        pkv.kv_cache_write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc, stream=stream, k_scale=ks, v_scale=vs)
+        decode()
+
+    ms, _ = timer.run(step, steps, warmup, sections=False)
+    launch_ms, _ = timer.run(lambda m: decode(), max(steps, 20), warmup, sections=False)
+    step_ms = sum(ms) / len(ms)
+    dec_ms = sum(launch_ms) / len(launch_ms)
+    return dict(step_ms=step_ms, launch_ms=dec_ms, kv_bytes=kv_bytes, alg_bytes=kv_bytes + other, R=R)
+
+
 def bench_decode_e2e(pkv, w, dev, stream, steps, warmup, timer):
     """The same step through the public API with host buffers: the step's inputs (q, new K/V,
     metadata) are copied from pinned host memory and out/lse read back, inside the timed region.
@@ -610,6 +642,22 @@ def main():
             del m
         except Exception as e:  # report, keep the headline
             extras["mixed_batch"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            r = bench_decode_fp8(pkv, dev, stream, timer, steps, warmup)
+            extras["decode_fp8"] = {
+                "workload": "the headline decode step over an FP8 (E4M3, per-tensor scale) cache: 256 seqs, "
+                            "ctx U[2000,3000], Hq 64 / Hkv 4, D 128; step = reorder + quantising kv_cache_write "
+                            "+ paged_decode_attn",
+                "kv_bytes_per_step": r["kv_bytes"], "ms_per_step": r["step_ms"],
+                "kv_gbs": r["kv_bytes"] / (r["step_ms"] * 1e-3) / 1e9,
+                "decode_tokens_per_s": r["R"] / (r["step_ms"] * 1e-3),
+                "bf16_decode_tokens_per_s": w["b"].R / (step_ms * 1e-3),
+                "launch_ms": r["launch_ms"],
+                "roofline_frac": r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"],
+            }
+        except Exception as e:
+            extras["decode_fp8"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         for kind in ("prefill", "extend_long"):
             try:

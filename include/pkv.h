@@ -25,12 +25,19 @@
  *
  * The paged cache of one layer
  *   k and v each hold num_blocks blocks of block_size tokens; a token row holds
- *   num_kv_heads x head_dim bf16 values, heads outermost: element (blk, t, h, d) sits at
+ *   num_kv_heads x head_dim elements, heads outermost: element (blk, t, h, d) sits at
  *   blk * stride_block + (t * num_kv_heads + h) * head_dim + d. stride_block (elements)
  *   is >= block_size * num_kv_heads * head_dim, so K and V may share one allocation as
- *   [num_blocks, 2, block_size, num_kv_heads, head_dim]. Base pointers and
- *   stride_block * 2 bytes must be multiples of 16.
+ *   [num_blocks, 2, block_size, num_kv_heads, head_dim]. Base pointers and stride_block
+ *   elements must be multiples of 16 bytes.
  *   Slot s (a token position in the pool) is block s / block_size, row s % block_size.
+ *   Element type (kv_dtype): PKV_KV_BF16, or PKV_KV_FP8_E4M3 — one byte per element, the
+ *   OCP E4M3 code c standing for e4m3(c) * k_scale (K) or * v_scale (V). The vLLM blog
+ *   "rocm-attention-backend" (MLA section) reads such a cache with a dequantising gather
+ *   ("gather_and_maybe_dequant_cache"); its served models are FP8. kv_cache_write stores
+ *   E4M3(float(x) * (1.0f / scale)), rounded to the nearest code (ties to even) and saturated
+ *   at +-448; pack/unpack copy codes; paged_decode_attn dequantises as it reads (head_dim 128).
+ *   extend_attn does not take an FP8 cache (PKV_ERR_UNSUPPORTED).
  *
  * The batch (arrival order, the layout vLLM's model runner gives its attention backend)
  *   R requests; cu_q int32 [R+1]: request r owns query rows cu_q[r] .. cu_q[r+1]-1 of the
@@ -82,14 +89,20 @@ typedef enum {
 #define PKV_DEVERR_LEN 0x8u       /* a length beyond a host bound (max_seq_len, max_q_len, table) */
 #define PKV_DEVERR_TIMEOUT 0x10u  /* a pipeline wait gave up (a library bug; results are wrong) */
 
+#define PKV_KV_BF16 0
+#define PKV_KV_FP8_E4M3 1
+
 typedef struct {
-  void* k;              /* device bf16, see "The paged cache of one layer" */
+  void* k;              /* device, kv_dtype elements, see "The paged cache of one layer" */
   void* v;
   int64_t num_blocks;
   int32_t block_size;   /* tokens per block */
   int32_t num_kv_heads;
   int32_t head_dim;
   int64_t stride_block; /* elements between consecutive blocks */
+  int32_t kv_dtype;     /* PKV_KV_BF16 or PKV_KV_FP8_E4M3 */
+  float k_scale;        /* FP8: value of a K code = e4m3(code) * k_scale (> 0, finite) */
+  float v_scale;        /* FP8: value of a V code = e4m3(code) * v_scale; both ignored for bf16 */
 } pkv_cache;
 
 typedef struct {

@@ -19,9 +19,13 @@ DEVERR = {0x1: "slot", 0x2: "block", 0x4: "reqs", 0x8: "len", 0x10: "timeout"}
 CLASS_DECODE, CLASS_EXTEND, CLASS_PREFILL = 0, 1, 2
 
 
+KV_BF16, KV_FP8_E4M3 = 0, 1
+
+
 class PkvCache(ctypes.Structure):
     _fields_ = [("k", P), ("v", P), ("num_blocks", i64), ("block_size", i32),
-                ("num_kv_heads", i32), ("head_dim", i32), ("stride_block", i64)]
+                ("num_kv_heads", i32), ("head_dim", i32), ("stride_block", i64),
+                ("kv_dtype", i32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class PkvReqs(ctypes.Structure):

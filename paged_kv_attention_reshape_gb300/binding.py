@@ -49,18 +49,23 @@ def _need(t: torch.Tensor, dtype, name: str, contiguous: bool = True):
         raise PkvError(f"{name} must be contiguous")
 
 
-def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> "_lib.PkvCache":
-    """Describe one layer's paged cache: k_cache / v_cache bf16 [num_blocks, block_size, Hkv, D]
-    with contiguous blocks (any stride between blocks)."""
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: float = 1.0,
+               v_scale: float = 1.0) -> "_lib.PkvCache":
+    """Describe one layer's paged cache: k_cache / v_cache [num_blocks, block_size, Hkv, D]
+    with contiguous blocks (any stride between blocks). bf16 tensors are a bf16 cache; uint8
+    or float8_e4m3fn tensors are an FP8 (E4M3) cache whose codes stand for e4m3(code) * scale."""
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    want = k_cache.dtype if fp8 else torch.bfloat16
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, torch.bfloat16, n, contiguous=False)
+        _need(t, want, n, contiguous=False)
         nb, bs, hkv, d = t.shape
         if t.stride()[1:] != (hkv * d, d, 1):
             raise PkvError(f"{n}: each block must be contiguous [block_size, Hkv, D]")
     if k_cache.shape != v_cache.shape or k_cache.stride(0) != v_cache.stride(0):
         raise PkvError("k_cache and v_cache must have the same shape and block stride")
     nb, bs, hkv, d = k_cache.shape
-    return _lib.PkvCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, k_cache.stride(0))
+    return _lib.PkvCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, k_cache.stride(0),
+                         _lib.KV_FP8_E4M3 if fp8 else _lib.KV_BF16, float(k_scale), float(v_scale))
 
 
 @dataclass
@@ -79,13 +84,14 @@ class Reqs:
                             self.cls, self.max_reqs, self.batch_reqs)
 
 
-def kv_cache_write(key, value, slot_mapping, k_cache, v_cache, stream=None):
-    """Scatter key/value [T, Hkv, D] into the cache slots given by slot_mapping (int64 [T])."""
+def kv_cache_write(key, value, slot_mapping, k_cache, v_cache, stream=None, k_scale=1.0, v_scale=1.0):
+    """Scatter key/value [T, Hkv, D] into the cache slots given by slot_mapping (int64 [T]);
+    into an FP8 cache, quantised with the per-tensor scales."""
     lib = _lib.load()
     _need(key, torch.bfloat16, "key")
     _need(value, torch.bfloat16, "value")
     _need(slot_mapping, torch.int64, "slot_mapping")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     _check(lib.pkv_kv_cache_write(_ptr(key), _ptr(value), _ptr(slot_mapping), slot_mapping.numel(),
                                   cache, _stream(stream)), "kv_cache_write")
 
@@ -97,8 +103,8 @@ def kv_block_pack(k_cache, v_cache, block_ids, dst=None, stream=None):
     cache = make_cache(k_cache, v_cache)
     n = block_ids.numel()
     if dst is None:
-        dst = torch.empty((2, n) + tuple(k_cache.shape[1:]), dtype=torch.bfloat16, device=k_cache.device)
-    _need(dst, torch.bfloat16, "dst")
+        dst = torch.empty((2, n) + tuple(k_cache.shape[1:]), dtype=k_cache.dtype, device=k_cache.device)
+    _need(dst, k_cache.dtype, "dst")
     _check(lib.pkv_kv_block_pack(cache, _ptr(block_ids), n, _ptr(dst), _stream(stream)), "kv_block_pack")
     return dst
 
@@ -106,7 +112,7 @@ def kv_block_pack(k_cache, v_cache, block_ids, dst=None, stream=None):
 def kv_block_unpack(src, block_ids, k_cache, v_cache, stream=None):
     """k_cache[block_ids[i]] = src[0][i], v_cache[block_ids[i]] = src[1][i] (in place)."""
     lib = _lib.load()
-    _need(src, torch.bfloat16, "src")
+    _need(src, k_cache.dtype, "src")
     _need(block_ids, torch.int32, "block_ids")
     cache = make_cache(k_cache, v_cache)
     n = block_ids.numel()
@@ -148,13 +154,14 @@ def paged_decode_workspace_size(max_reqs, Hq, Hkv, D, max_seq_len) -> int:
 
 def paged_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, cu_q=None,
                       reqs: Optional[Reqs] = None, scale=None, out=None, lse=None, workspace=None,
-                      stream=None):
-    """One query token per request against its paged context. q [T, Hq, D]."""
+                      stream=None, k_scale=1.0, v_scale=1.0):
+    """One query token per request against its paged context. q [T, Hq, D]. An FP8 cache is
+    dequantised with the per-tensor scales as it is read."""
     lib = _lib.load()
     _need(q, torch.bfloat16, "q")
     _need(block_tables, torch.int32, "block_tables")
     _need(seq_lens, torch.int32, "seq_lens")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     T, Hq, D = q.shape
     R = seq_lens.numel()
     reqs = reqs or Reqs(max_reqs=R, batch_reqs=R)
@@ -173,7 +180,8 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, 
 
 
 def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, out, lse,
-                              cu_q=None, reqs: Optional[Reqs] = None, scale=None, stream=None):
+                              cu_q=None, reqs: Optional[Reqs] = None, scale=None, stream=None,
+                              k_scale=1.0, v_scale=1.0):
     """paged_decode_attn for callers that cannot allocate: the library uses its own fixed
     device scratch (NOALLOC_SCRATCH_BYTES per GPU) and the caller passes out and lse."""
     lib = _lib.load()
@@ -182,7 +190,7 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_s
     _need(lse, torch.float32, "lse")
     _need(block_tables, torch.int32, "block_tables")
     _need(seq_lens, torch.int32, "seq_lens")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     T, Hq, D = q.shape
     R = seq_lens.numel()
     reqs = reqs or Reqs(max_reqs=R, batch_reqs=R)

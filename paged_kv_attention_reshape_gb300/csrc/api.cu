@@ -67,6 +67,8 @@ uint32_t next_epoch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int64_t elem_bytes(const pkv_cache& c) { return c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2; }
+
 // TMA map over a token-major tensor [rows, heads, D] (bf16): dims (64, heads*D/64, rows),
 // box 64 x 1 x box_rows, 128-byte swizzle. One box = one 64-wide half of one head's rows.
 bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows) {
@@ -87,6 +89,19 @@ bool encode_cache(CUtensorMap* m, const void* base, const pkv_cache& c) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const int D = c.head_dim;
+  if (c.kv_dtype == PKV_KV_FP8_E4M3) {
+    // one byte per element: dims (D, Hkv, block_size, num_blocks), box D x 1 x block_size x 1
+    // (one head of one block; 128 bytes per row at D = 128), 128-byte swizzle
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(c.num_kv_heads),
+                          static_cast<cuuint64_t>(c.block_size), static_cast<cuuint64_t>(c.num_blocks)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(c.num_kv_heads) * D,
+                             static_cast<cuuint64_t>(c.stride_block)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(c.block_size), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(c.num_kv_heads) * (D / 64),
                         static_cast<cuuint64_t>(c.block_size), static_cast<cuuint64_t>(c.num_blocks)};
   cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(c.num_kv_heads) * D * 2,
@@ -109,13 +124,19 @@ pkv_status check_cache(const pkv_cache& c, bool attention) {
   if (c.k == nullptr || c.v == nullptr || c.num_blocks <= 0 || c.block_size <= 0 ||
       c.num_kv_heads <= 0 || c.head_dim <= 0)
     return PKV_ERR_INVALID_ARG;
+  if (c.kv_dtype != PKV_KV_BF16 && c.kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+  if (c.kv_dtype == PKV_KV_FP8_E4M3 &&
+      !(std::isfinite(c.k_scale) && c.k_scale > 0.f && std::isfinite(c.v_scale) && c.v_scale > 0.f))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t esize = elem_bytes(c);
   if (!aligned16(c.k) || !aligned16(c.v)) return PKV_ERR_INVALID_ARG;
   const int64_t blk_elems = static_cast<int64_t>(c.block_size) * c.num_kv_heads * c.head_dim;
-  if (c.stride_block < blk_elems || (c.stride_block * 2) % 16 != 0) return PKV_ERR_INVALID_ARG;
-  if ((static_cast<int64_t>(c.num_kv_heads) * c.head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (c.stride_block < blk_elems || (c.stride_block * esize) % 16 != 0) return PKV_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(c.num_kv_heads) * c.head_dim * esize) % 16 != 0) return PKV_ERR_UNSUPPORTED;
   if (attention) {
     if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (c.block_size != 16) return PKV_ERR_UNSUPPORTED;
+    if (c.kv_dtype == PKV_KV_FP8_E4M3 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
   }
   return PKV_OK;
 }
@@ -231,7 +252,7 @@ pkv_status pkv_kv_block_pack(pkv_cache cache, const int32_t* block_ids, int32_t 
   if (st != PKV_OK) return st;
   if (num_ids == 0) return PKV_OK;
   if (block_ids == nullptr || dst == nullptr || !aligned16(dst)) return PKV_ERR_INVALID_ARG;
-  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * 2) % 16 != 0)
+  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * elem_bytes(cache)) % 16 != 0)
     return PKV_ERR_UNSUPPORTED;
   if (num_ids > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
   st = cuda_status(launch_kv_block_pack(cache, block_ids, num_ids, dst, error_word(),
@@ -247,7 +268,7 @@ pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_
   if (st != PKV_OK) return st;
   if (num_ids == 0) return PKV_OK;
   if (block_ids == nullptr || src == nullptr || !aligned16(src)) return PKV_ERR_INVALID_ARG;
-  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * 2) % 16 != 0)
+  if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * elem_bytes(cache)) % 16 != 0)
     return PKV_ERR_UNSUPPORTED;
   if (num_ids > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
   st = cuda_status(launch_kv_block_unpack(src, block_ids, num_ids, cache, error_word(),
@@ -316,7 +337,11 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   p.G = num_q_heads / cache.num_kv_heads;
   p.num_blocks = cache.num_blocks;
   p.max_seq_len = max_seq_len;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  const bool fp8 = cache.kv_dtype == PKV_KV_FP8_E4M3;
+  // an FP8 cache holds codes: the key scale folds into the softmax scale, the value scale
+  // into the output
+  p.scale_log2 = scale * (fp8 ? cache.k_scale : 1.f) * 1.4426950408889634f;
+  p.v_scale = fp8 ? cache.v_scale : 1.f;
   const size_t need = decode_workspace_bytes(p.Hq, p.Hkv, cache.head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   p.ws_part = static_cast<float*>(workspace);
@@ -326,7 +351,7 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   CUtensorMap tk, tv;
   if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
   int launches = 0;
-  st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim,
+  st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim, fp8,
                                        reinterpret_cast<cudaStream_t>(stream), &launches));
   t_launches += launches;
   return st;
@@ -344,6 +369,7 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   pkv_status st = check_reqs(reqs);
   if (st != PKV_OK) return st;
   if (cache != nullptr && (st = check_cache(*cache, true)) != PKV_OK) return st;
+  if (cache != nullptr && cache->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   if (!group_ok(Hq, Hkv)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale))

@@ -37,13 +37,17 @@
 
 namespace pkv {
 
-template <int D>
+// FP8: the cache holds E4M3 codes (one byte per element). A block row of one head is then
+// D bytes (one 128-byte TMA box at D = 128), a stage half as large, and twice as many stages
+// keep the same bytes in flight per warp in the same shared memory.
+template <int D, bool FP8 = false>
 struct DecodeCfg {
   static constexpr int MAXW = 8;                      // warps (KV heads) per CTA, at most
-  static constexpr int NSW = 2;                       // ring stages per warp
+  static constexpr int NSW = FP8 ? 4 : 2;             // ring stages per warp
   static constexpr int BS = 16;                       // tokens per block
-  static constexpr int HALVES = D / 64;               // 64-element (128-byte) column halves
-  static constexpr int TILE_BYTES = BS * D * 2;       // one block of K (or V) for one head
+  static constexpr int EB = FP8 ? 1 : 2;              // bytes per cached element
+  static constexpr int HALVES = FP8 ? 1 : D / 64;     // 128-byte column boxes per row
+  static constexpr int TILE_BYTES = BS * D * EB;      // one block of K (or V) for one head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
   static constexpr int Q_BYTES = 16 * D * 2;
   static constexpr int MAXR = 1024;     // requests per set handled on device
@@ -297,11 +301,12 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams& p, int64_t row,
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
+template <int D, bool FP8>
+__global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_kernel(
     const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
-  using C = DecodeCfg<D>;
+  using C = DecodeCfg<D, FP8>;
+  static_assert(!FP8 || D == 128, "FP8 cache rows are one 128-byte box");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nthreads = blockDim.x, nw = nthreads >> 5;
@@ -470,10 +475,15 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       uint8_t* sK = ring + stage * C::STAGE_BYTES;
       uint8_t* sV = sK + C::TILE_BYTES;
       mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+      if constexpr (FP8) {
+        tma_load_4d(sK, &tm_k, &full[stage], 0, kh, 0, blk);
+        tma_load_4d(sV, &tm_v, &full[stage], 0, kh, 0, blk);
+      } else {
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_4d(sK + h * 2048, &tm_k, &full[stage], 0, kh * C::HALVES + h, 0, blk);
-        tma_load_4d(sV + h * 2048, &tm_v, &full[stage], 0, kh * C::HALVES + h, 0, blk);
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_4d(sK + h * 2048, &tm_k, &full[stage], 0, kh * C::HALVES + h, 0, blk);
+          tma_load_4d(sV + h * 2048, &tm_v, &full[stage], 0, kh * C::HALVES + h, 0, blk);
+        }
       }
     }
     ++lj;
@@ -533,6 +543,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       for (int ks = 0; ks < D / 16; ++ks)
         ldsm_x4(qbase + (ks / 4) * 2048 + sw128(lane & 15, (ks % 4) * 2 + (lane >> 4)), qa[ks][0], qa[ks][1],
                 qa[ks][2], qa[ks][3]);
+      if constexpr (FP8) {  // the FP8 path multiplies in fp16: E4M3 codes convert to it exactly
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qa[ks][i] = bf16x2_to_f16x2(qa[ks][i]);
+      }
     }
     __syncwarp();
     {
@@ -557,6 +573,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       const int valid = min(C::BS, ctx - j * C::BS);  // tokens of this block
       if (valid < C::BS) {
         // zero the V rows past the end so that P = 0 there cannot meet a non-finite value
+        // (whole 128-byte rows: the swizzle only permutes chunks within a row)
         for (int c = lane; c < (C::BS - valid) * C::HALVES * 8; c += 32) {
           const int rrow = valid + c / (C::HALVES * 8);
           const int rest = c % (C::HALVES * 8);
@@ -566,15 +583,32 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
       }
       // S = Q K^T : 16 rows x 16 tokens as two 8-token n-tiles
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint32_t kbase = smem_u32(sK);
+      if constexpr (FP8) {
+        // B fragment of token n = 8 nt + lane/4, dims 16 ks + 2 (lane % 4) + {0, 1} (+ 8): two
+        // code pairs of the token's 128-byte row (16-byte chunk ks, swizzled by the row)
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int tok = ((lane >> 4) << 3) + (lane & 7);
-        const int chunk = (ks % 4) * 2 + ((lane >> 3) & 1);
-        uint32_t b0r, b1r, b2r, b3r;
-        ldsm_x4(kbase + (ks / 4) * 2048 + sw128(tok, chunk), b0r, b1r, b2r, b3r);
-        mma_16816(sc[0], qa[ks], b0r, b1r);
-        mma_16816(sc[1], qa[ks], b2r, b3r);
+        for (int nt = 0; nt < 2; ++nt) {
+          const int tok = nt * 8 + (lane >> 2);
+          const uint8_t* rowp = sK + tok * 128 + 2 * (lane & 3);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint8_t* cp = rowp + ((ks ^ (tok & 7)) << 4);
+            const uint32_t b0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(cp));
+            const uint32_t b1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(cp + 8));
+            mma_16816_f16(sc[nt], qa[ks], b0, b1);
+          }
+        }
+      } else {
+        const uint32_t kbase = smem_u32(sK);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int tok = ((lane >> 4) << 3) + (lane & 7);
+          const int chunk = (ks % 4) * 2 + ((lane >> 3) & 1);
+          uint32_t b0r, b1r, b2r, b3r;
+          ldsm_x4(kbase + (ks / 4) * 2048 + sw128(tok, chunk), b0r, b1r, b2r, b3r);
+          mma_16816(sc[0], qa[ks], b0r, b1r);
+          mma_16816(sc[1], qa[ks], b2r, b3r);
+        }
       }
       // online softmax in log2 units: max over raw scores (the scale is positive), then
       // p = 2^(s * scale_log2 - m) with one FFMA
@@ -616,20 +650,38 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
         o[i][3] *= alpha[1];
       }
       uint32_t pa[4];
-      pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-      pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-      pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-      pa[3] = pack_bf16(sc[1][2], sc[1][3]);
-      // O += P V
-      const uint32_t vbase = smem_u32(sV);
+      if constexpr (FP8) {
+        pa[0] = pack_f16(sc[0][0], sc[0][1]);
+        pa[1] = pack_f16(sc[0][2], sc[0][3]);
+        pa[2] = pack_f16(sc[1][0], sc[1][1]);
+        pa[3] = pack_f16(sc[1][2], sc[1][3]);
+        // O += P V: the B fragment of dim n = 8 nt + lane/4 holds tokens 2 (lane % 4) + {0, 1}
+        // (+ 8): four codes from four token rows, paired and converted to fp16
+        const int t0 = 2 * (lane & 3);
 #pragma unroll
-      for (int nd = 0; nd < D / 16; ++nd) {
-        const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
-        const int d = nd * 16 + ((lane >> 4) << 3);
-        uint32_t b0r, b1r, b2r, b3r;
-        ldsm_x4_t(vbase + (d / 64) * 2048 + sw128(tok, (d % 64) / 8), b0r, b1r, b2r, b3r);
-        mma_16816(o[2 * nd], pa, b0r, b1r);
-        mma_16816(o[2 * nd + 1], pa, b2r, b3r);
+        for (int nt = 0; nt < D / 8; ++nt) {
+          const int n = nt * 8 + (lane >> 2);
+          auto code = [&](int tok) { return static_cast<uint32_t>(sV[tok * 128 + (((n >> 4) ^ (tok & 7)) << 4) + (n & 15)]); };
+          const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(code(t0) | (code(t0 + 1) << 8)));
+          const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(code(t0 + 8) | (code(t0 + 9) << 8)));
+          mma_16816_f16(o[nt], pa, b0, b1);
+        }
+      } else {
+        pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+        pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+        pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+        pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+        // O += P V
+        const uint32_t vbase = smem_u32(sV);
+#pragma unroll
+        for (int nd = 0; nd < D / 16; ++nd) {
+          const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
+          const int d = nd * 16 + ((lane >> 4) << 3);
+          uint32_t b0r, b1r, b2r, b3r;
+          ldsm_x4_t(vbase + (d / 64) * 2048 + sw128(tok, (d % 64) / 8), b0r, b1r, b2r, b3r);
+          mma_16816(o[2 * nd], pa, b0r, b1r);
+          mma_16816(o[2 * nd + 1], pa, b2r, b3r);
+        }
       }
       // the stage's reads (and any zeroing) are done: refill it with the block NSW ahead
       fence_proxy_async_smem();
@@ -652,7 +704,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
     float inv[2], lse[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+      inv[h] = l_run[h] > 0.f ? p.v_scale / l_run[h] : 0.f;  // the value scale of an FP8 cache folds in
       lse[h] = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
     }
     if (whole) {
@@ -720,6 +772,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::MAXW * 32) paged_decode_kernel(
 // block, less room for the kernel's few static shared variables.
 static int max_dyn_smem() { return max_smem_optin() - 1024; }
 
+static_assert(DecodeCfg<128, true>::WARP_BYTES == DecodeCfg<128>::WARP_BYTES,
+              "the FP8 and bf16 decode take the same launch shape");
 // Launch shape: warps per CTA = KV heads per CTA (at most 8); about 8 warps per SM.
 struct DecodeShape {
   int nw, groups, shares;
@@ -748,15 +802,15 @@ size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
          static_cast<size_t>(decode_shape(Hkv).shares) * Hkv * sizeof(unsigned long long);
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& tk,
                                       const CUtensorMap& tv, cudaStream_t stream, int* launches) {
-  using C = DecodeCfg<D>;
-  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D>), max_dyn_smem(),
-                                     D == 64 ? kAttrDecode64 : kAttrDecode128);
+  using C = DecodeCfg<D, FP8>;
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D, FP8>), max_dyn_smem(),
+                                     FP8 ? kAttrDecode128Fp8 : (D == 64 ? kAttrDecode64 : kAttrDecode128));
   if (e != cudaSuccess) return e;
   const DecodeShape sh = decode_shape(p.Hkv);
-  e = launch_pdl(paged_decode_kernel<D>, dim3(sh.shares, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
+  e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(sh.shares, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
                  p, tk, tv);
   *launches += 1;
   return e;
@@ -767,9 +821,10 @@ int decode_smem_bytes(int D) {
 }
 
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                int D, cudaStream_t stream, int* launches) {
-  return D == 64 ? launch_decode_impl<64>(p, tk, tv, stream, launches)
-                 : launch_decode_impl<128>(p, tk, tv, stream, launches);
+                                int D, bool fp8, cudaStream_t stream, int* launches) {
+  if (fp8) return launch_decode_impl<128, true>(p, tk, tv, stream, launches);
+  return D == 64 ? launch_decode_impl<64, false>(p, tk, tv, stream, launches)
+                 : launch_decode_impl<128, false>(p, tk, tv, stream, launches);
 }
 
 }  // namespace pkv

@@ -28,7 +28,8 @@ struct DecodeParams {
   int32_t Hq, Hkv, G;
   int64_t num_blocks;
   int32_t max_seq_len;
-  float scale_log2;      // softmax scale * log2(e)
+  float scale_log2;      // softmax scale * log2(e) (times the key scale for an FP8 cache)
+  float v_scale;         // FP8 cache: value of a V code = e4m3(code) * v_scale; 1 for bf16
   float* ws_part;        // [shares][2][Hkv][G][D + 4] partials of sequences cut at share edges
   unsigned long long* ws_ctr;  // [shares][Hkv] arrival counters of cut sequences: epoch << 32 | count
   uint32_t epoch;        // distinct per call: counters left by earlier calls read as empty
@@ -79,6 +80,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 enum AttrSlot {
   kAttrDecode64 = 0,
   kAttrDecode128,
+  kAttrDecode128Fp8,
   kAttrAttn64,
   kAttrAttn128,
   kAttrCount
@@ -102,7 +104,7 @@ cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* se
                                           int32_t* cu_q_reordered, int32_t* token_map,
                                           int64_t num_tokens, cudaStream_t stream, int* launches);
 cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                int D, cudaStream_t stream, int* launches);
+                                int D, bool fp8, cudaStream_t stream, int* launches);
 int decode_smem_bytes(int D);
 size_t decode_workspace_bytes(int Hq, int Hkv, int D);
 size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D);

@@ -235,6 +235,19 @@ def write_pack_layers(num_layers: int, T: int, *, Hkv: int, D: int, block_size: 
     return layers
 
 
+def fp8_codes(t: torch.Tensor, scale: float) -> torch.Tensor:
+    """E4M3 codes (uint8, same shape and device) standing for t / scale: an FP8 cache's content
+    synthesised from values, with torch's float8_e4m3fn conversion (round to nearest even) after
+    clamping to the finite range. Input synthesis only: the library's quantiser is not used."""
+    x = (t.float() / scale).clamp_(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def fp8_scale(amax: float) -> float:
+    """Per-tensor scale mapping |x| <= amax onto the E4M3 range."""
+    return float(amax) / 448.0
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bits of a bf16 tensor as a host uint16 array (the oracle's input format)."""
     assert t.dtype == torch.bfloat16

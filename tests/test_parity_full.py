@@ -51,6 +51,34 @@ def test_decode_qwen3_full(pkv):
     print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="decode qwen3 full"))
 
 
+def test_decode_qwen3_fp8_full(pkv):
+    """The headline workload over an FP8 (E4M3) cache: the caches hold codes, the new tokens
+    are quantised by kv_cache_write, decode dequantises as it reads; the written caches bit for
+    bit, 24 sampled sequences against the oracle."""
+    b = gen.decode_batch(**gen.DECODE_QWEN3, device="cuda")
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    del b.k_cache, b.v_cache
+    kc0, vc0 = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+    R = b.R
+    perm, bounds, _, _ = pkv.batch_classify_reorder(b.cu_q, b.seq_lens)
+    pkv.kv_cache_write(b.k_new, b.v_new, b.slot_mapping, kc, vc, k_scale=ks, v_scale=vs)
+    out, lse = pkv.paged_decode_attn(b.q, kc, vc, b.block_tables, b.seq_lens, max(b.seq_lens_list), cu_q=b.cu_q,
+                                     reqs=pkv.Reqs(R, R, perm, bounds, pkv.CLASS_DECODE),
+                                     scale=1 / math.sqrt(b.D), k_scale=ks, v_scale=vs)
+    assert pkv.device_errors() == 0
+    assert oracle.kv_cache_write_fp8(_host(b.k_new), _host(b.v_new), b.slot_mapping.cpu().numpy(), kc0, vc0,
+                                     ks, vs) == 0
+    assert np.array_equal(kc.cpu().numpy(), kc0) and np.array_equal(vc.cpu().numpy(), vc0)
+    sample = np.sort(np.random.default_rng(0).choice(R, 24, replace=False)).astype(np.int32)
+    ref, ref_lse = oracle.paged_decode_fp8(_host(b.q), kc0, vc0, b.block_tables.cpu().numpy(),
+                                           b.seq_lens.cpu().numpy(), 1 / math.sqrt(b.D), ks, vs,
+                                           cu_q=b.cu_q.cpu().numpy(), req_ids=sample)
+    rows = np.zeros(b.T, bool)
+    rows[sample] = True
+    print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="decode qwen3 fp8 full"))
+
+
 def test_mixed_llama70b_full(pkv):
     """192 decode + 8 extend (512 over 4k-32k) + 4 prefill (2k-8k), shuffled: the full step;
     sampled rows of every class checked."""

@@ -132,6 +132,105 @@ def test_kv_block_unpack_strided_cache_and_bad_ids(pkv):
     assert _errors(pkv) & 0x2
 
 
+# ---- FP8 (E4M3) cache -----------------------------------------------------------------------------
+
+def _codes(t):
+    return t.detach().contiguous().cpu().view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("Hkv,D", [(8, 128), (4, 128), (2, 64), (1, 16)])
+def test_kv_cache_write_fp8_bit_exact(pkv, Hkv, D):
+    """Quantising write: code = E4M3(float(x) * (1/scale)), round to nearest even, saturating;
+    bit for bit the oracle's (which is pinned to torch's float8 conversion)."""
+    L = gen.write_pack_layers(1, 300, Hkv=Hkv, D=D, seed=40 + Hkv)[0]
+    nb = L.k_cache.shape[0]
+    g = torch.Generator().manual_seed(41)
+    kc0 = torch.randint(0, 0x7F, (nb, 16, Hkv, D), generator=g, dtype=torch.uint8)
+    vc0 = torch.randint(0x80, 0xFF, (nb, 16, Hkv, D), generator=g, dtype=torch.uint8)
+    ks, vs = 0.0213, 0.00071   # the V scale saturates the larger values at +-448
+    gk, gv = kc0.to(DEV), vc0.to(DEV)
+    pkv.kv_cache_write(L.key.to(DEV), L.value.to(DEV), L.slot_mapping.to(DEV), gk, gv, k_scale=ks, v_scale=vs)
+    ek, ev = kc0.numpy().copy(), vc0.numpy().copy()
+    assert oracle.kv_cache_write_fp8(bits(L.key), bits(L.value), L.slot_mapping.numpy(), ek, ev, ks, vs) == 0
+    assert np.array_equal(_codes(gk), ek) and np.array_equal(_codes(gv), ev)
+    assert (ev == 0x7E).any() or (ev == 0xFE).any()   # saturation exercised
+    assert _errors(pkv) == 0
+
+
+def test_kv_block_pack_unpack_fp8_bit_exact(pkv):
+    g = torch.Generator().manual_seed(42)
+    nb, n = 200, 61
+    kc = torch.randint(0, 256, (nb, 16, 4, 128), generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 256, (nb, 16, 4, 128), generator=g, dtype=torch.uint8)
+    ids = torch.randperm(nb, generator=g)[:n].to(torch.int32)
+    dst_ids = torch.randperm(nb, generator=g)[:n].to(torch.int32)
+    packed = pkv.kv_block_pack(kc.to(DEV), vc.to(DEV), ids.to(DEV))
+    assert packed.dtype == torch.uint8
+    assert np.array_equal(_codes(packed[0]), kc.numpy()[ids.numpy()])
+    assert np.array_equal(_codes(packed[1]), vc.numpy()[ids.numpy()])
+    rk, rv = torch.zeros_like(kc).to(DEV), torch.zeros_like(vc).to(DEV)
+    pkv.kv_block_unpack(packed, dst_ids.to(DEV), rk, rv)
+    ek, ev = np.zeros_like(kc.numpy()), np.zeros_like(vc.numpy())
+    ek[dst_ids.numpy()] = kc.numpy()[ids.numpy()]
+    ev[dst_ids.numpy()] = vc.numpy()[ids.numpy()]
+    assert np.array_equal(_codes(rk), ek) and np.array_equal(_codes(rv), ev)
+
+
+def _fp8_decode_case(B, lo, hi, Hq, Hkv, seed, q_scale=1.0):
+    b = gen.decode_batch(B, lo, hi, Hq=Hq, Hkv=Hkv, D=128, seed=seed, q_scale=q_scale)
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    return b, gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs), ks, vs
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_decode_fp8_group_sizes(pkv, G):
+    b, kc, vc, ks, vs = _fp8_decode_case(5, 1, 300, Hq=2 * G, Hkv=2, seed=50 + G)
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), kc.to(DEV), vc.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(b.seq_lens_list), scale=1 / math.sqrt(128),
+                                     k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc), _codes(vc), b.block_tables.numpy(),
+                                           b.seq_lens.numpy(), 1 / math.sqrt(128), ks, vs)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode fp8 G={G}")
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("ctxs", [[1, 16, 17, 31, 32, 33], [4096, 1, 7000, 15]])
+def test_decode_fp8_edge_lengths_and_nan_codes_past_the_end(pkv, ctxs):
+    """Ragged and cut sequences; codes past each sequence's end are NaN codes (0x7F), which
+    must not reach the result."""
+    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=32, Hkv=4, D=128, seed=60)
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.0)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    for r, n in enumerate(ctxs):
+        last = int(b.block_tables[r, (n - 1) // 16])
+        kc[last, (n - 1) % 16 + 1:] = 0x7F
+        vc[last, (n - 1) % 16 + 1:] = 0x7F
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), kc.to(DEV), vc.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(ctxs), scale=1 / math.sqrt(128), k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc), _codes(vc), b.block_tables.numpy(),
+                                           b.seq_lens.numpy(), 1 / math.sqrt(128), ks, vs)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, what="decode fp8 edges")
+
+
+def test_decode_fp8_peaked_softmax(pkv):
+    b, kc, vc, ks, vs = _fp8_decode_case(8, 100, 2000, Hq=64, Hkv=4, seed=61, q_scale=4.0)
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), kc.to(DEV), vc.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(b.seq_lens_list), scale=1 / math.sqrt(128),
+                                     k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc), _codes(vc), b.block_tables.numpy(),
+                                           b.seq_lens.numpy(), 1 / math.sqrt(128), ks, vs)
+    compare_attention(out, lse, ref, ref_lse, what="decode fp8 peaked")
+
+
+def test_extend_rejects_fp8_cache(pkv):
+    b = gen.extend_batch([5], [20], Hq=8, Hkv=2, D=128, seed=62)
+    kc = torch.zeros(tuple(b.k_cache.shape), dtype=torch.uint8, device=DEV)
+    with pytest.raises(pkv.PkvError):
+        pkv.extend_attn(b.q.to(DEV), b.k_new.to(DEV), b.v_new.to(DEV), b.cu_q.to(DEV), b.seq_lens.to(DEV),
+                        kc, kc.clone(), b.block_tables.to(DEV), 5, 25)
+
+
 # ---- batch_classify_reorder ------------------------------------------------------------------
 
 def _reorder_case(R, seed, thr=1):

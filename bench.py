@@ -293,32 +293,49 @@ def bench_decode_fp8(pkv, dev, stream, timer, steps, warmup):
 
 
 def bench_decode_e2e(pkv, w, dev, stream, steps, warmup, timer):
-    """The same step through the public API with host buffers: the step's inputs (q, new K/V,
-    metadata) are copied from pinned host memory and out/lse read back, inside the timed region.
-    The KV cache stays resident (it is the state of the server)."""
+    """The same step through the public API with host buffers: every input of the step (q, the
+    new K/V, slot mapping, lengths, block tables) is copied from pinned host memory and out/lse
+    read back, inside the timed region. As a serving engine would, the step stages its inputs
+    in one pinned buffer and one device buffer (one host-to-device copy) and its outputs in one
+    device buffer (one device-to-host copy); the library calls take views into them. The KV
+    cache stays resident (it is the state of the server)."""
     b = w["b"]
-    hq = b.q.cpu().pin_memory()
-    hk = b.k_new.cpu().pin_memory()
-    hv = b.v_new.cpu().pin_memory()
-    hmeta = {k: v.cpu().pin_memory() for k, v in w["meta"].items()}
-    hout = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
-    hlse = torch.empty(w["lse"].shape, dtype=torch.float32).pin_memory()
-    dq, dk, dv = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
-    dmeta = {k: torch.empty_like(v) for k, v in w["meta"].items()}
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + sum(v.numel() * v.element_size() for v in hmeta.values())
-    d2h = hout.numel() * 2 + hlse.numel() * 4
+    parts = [("q", b.q), ("k_new", b.k_new), ("v_new", b.v_new)] + [(k, v) for k, v in w["meta"].items()]
+
+    def layout(tensors):
+        offs, off = {}, 0
+        for name, t in tensors:
+            off = (off + 255) // 256 * 256
+            offs[name] = (off, t.numel() * t.element_size())
+            off += offs[name][1]
+        return offs, off
+
+    in_offs, in_bytes = layout(parts)
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    for name, t in parts:
+        o, n = in_offs[name]
+        h_in[o:o + n].copy_(t.detach().contiguous().view(-1).view(torch.uint8).cpu())
+
+    def view(buf, offs, name, like):
+        o, n = offs[name]
+        return buf[o:o + n].view(like.dtype).view(like.shape)
+
+    dq, dk, dv = (view(d_in, in_offs, n, t) for n, t in parts[:3])
+    dmeta = {k: view(d_in, in_offs, k, v) for k, v in w["meta"].items()}
+    out_parts = [("out", w["out"]), ("lse", w["lse"])]
+    out_offs, out_bytes = layout(out_parts)
+    d_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    dout, dlse = view(d_out, out_offs, "out", w["out"]), view(d_out, out_offs, "lse", w["lse"])
+    h2d, d2h = in_bytes, out_bytes
 
     def step():
         with torch.cuda.stream(stream):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            for k in dmeta:
-                dmeta[k].copy_(hmeta[k], non_blocking=True)
-        decode_step(pkv, w, stream, None, q=dq, meta=dmeta, k_new=dk, v_new=dv)
+            d_in.copy_(h_in, non_blocking=True)
+        decode_step(pkv, w, stream, None, q=dq, meta=dmeta, k_new=dk, v_new=dv, out=dout, lse=dlse)
         with torch.cuda.stream(stream):
-            hout.copy_(w["out"], non_blocking=True)
-            hlse.copy_(w["lse"], non_blocking=True)
+            h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(warmup):
         step()

@@ -295,6 +295,16 @@ pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_
  * ------------------------------------------------------------------------------------- */
 pkv_status pkv_device_errors(uint32_t* flags, int32_t clear, pkv_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * pkv_selftest_bounded_wait — exercise the failure path of the library's pipeline waits.
+ * Enqueues one small kernel that waits on a shared-memory barrier nothing will complete, with
+ * the library's bounded wait cut to limit_ns (1 us .. 2 s): the wait gives up, the kernel sets
+ * PKV_DEVERR_TIMEOUT in the device error word and exits, and the context stays usable. The
+ * pages have no counterpart; it lets callers and tests see a wait run out without faulting or
+ * hanging the GPU.
+ * ------------------------------------------------------------------------------------- */
+pkv_status pkv_selftest_bounded_wait(uint64_t limit_ns, pkv_stream_t stream);
+
 /* Number of kernels the library enqueued on this host thread since the last reset (host
  * counter; used by benchmarks to report launches). reset != 0 zeroes it after reading. */
 int64_t pkv_launch_count(int32_t reset);

@@ -121,6 +121,12 @@ def kv_block_unpack(src, block_ids, k_cache, v_cache, stream=None):
     _check(lib.pkv_kv_block_unpack(_ptr(src), _ptr(block_ids), n, cache, _stream(stream)), "kv_block_unpack")
 
 
+def selftest_bounded_wait(limit_ns=10_000_000, stream=None):
+    """Run a kernel whose barrier wait must run out after limit_ns (sets the TIMEOUT bit of the
+    device error word; the context stays usable)."""
+    _check(_lib.load().pkv_selftest_bounded_wait(int(limit_ns), _stream(stream)), "selftest_bounded_wait")
+
+
 def batch_classify_reorder(cu_q, seq_lens, decode_threshold=1, perm=None, bounds=None,
                            cu_q_reordered=None, token_map=None, with_token_map=False,
                            num_tokens=None, stream=None):

@@ -1,6 +1,6 @@
 // api.cu — the C ABI (include/pkv.h): host-side argument checks, TMA descriptor encoding,
-// launch-shape heuristics and the per-device error word. Every compute step runs in the
-// kernels of the other files; nothing here touches tensor data.
+// launch-shape heuristics, the per-device error word and the bounded-wait self-test kernel.
+// Every compute step runs in the kernels of the other files; nothing here touches tensor data.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -8,6 +8,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "common.cuh"
 #include "launch.h"
 
 namespace pkv {
@@ -197,6 +198,23 @@ cudaError_t set_smem_attr_once(const void* func, int bytes, int slot) {
 
 using namespace pkv;
 
+namespace pkv {
+// One barrier that nothing arrives on; the bounded wait gives up after limit_ns and flags
+// PKV_DEVERR_TIMEOUT, exactly as a stalled pipeline wait in the kernels would.
+__global__ void selftest_wait_kernel(unsigned int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  pdl_wait();
+  pdl_release();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_limit(&bar, 0, err, limit_ns));
+  (void)ok;
+}
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_status_string(pkv_status s) {
@@ -209,6 +227,14 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_DEVICE: return "device-side index error";
   }
   return "unknown status";
+}
+
+pkv_status pkv_selftest_bounded_wait(uint64_t limit_ns, pkv_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > kWaitLimitNs) return PKV_ERR_INVALID_ARG;
+  const cudaError_t e = launch_pdl(selftest_wait_kernel, dim3(1), dim3(32), 0,
+                                   reinterpret_cast<cudaStream_t>(stream), error_word(), limit_ns);
+  t_launches += 1;
+  return cuda_status(e);
 }
 
 int64_t pkv_launch_count(int32_t reset) {

@@ -69,16 +69,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Wait for the phase with the given parity to complete, for at most ~2 s of wall time.
 // Returns false (and flags PKV_DEVERR_TIMEOUT) when it gives up.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       flag_error(err, PKV_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+  return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
 // ---- TMA ----------------------------------------------------------------------------------

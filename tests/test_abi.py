@@ -78,6 +78,9 @@ def test_host_checks_reject_bad_arguments_without_a_gpu(lib):
     assert lib.pkv_kv_block_unpack(P((1 << 20) + 4), fake, 3, cache, None) == 1
     assert lib.pkv_kv_block_unpack(fake, fake, -1, cache, None) == 1
     assert lib.pkv_kv_block_unpack(None, None, 0, cache, None) == 0
+    # self-test wait limits outside 1 us .. 2 s
+    assert lib.pkv_selftest_bounded_wait(10, None) == 1
+    assert lib.pkv_selftest_bounded_wait(3_000_000_000, None) == 1
     # token map without reordered starts
     assert lib.pkv_batch_classify_reorder(fake, fake, 4, 1, fake, fake, None, fake, 10, None) == 1
     # identity set larger than the batch

@@ -231,6 +231,22 @@ def test_extend_rejects_fp8_cache(pkv):
                         kc, kc.clone(), b.block_tables.to(DEV), 5, 25)
 
 
+# ---- failure detection -----------------------------------------------------------------------
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(pkv):
+    """A barrier nothing completes: the library's bounded wait gives up after the limit, the
+    TIMEOUT bit shows in the device error word, and the next calls run normally."""
+    pkv.device_errors(clear=True)
+    pkv.selftest_bounded_wait(limit_ns=20_000_000)
+    assert pkv.device_errors(clear=True) & 0x10
+    b = gen.decode_batch(**gen.TINY_DECODE)
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), b.k_cache.to(DEV), b.v_cache.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(b.seq_lens_list), scale=1 / math.sqrt(b.D))
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), 1 / math.sqrt(b.D))
+    compare_attention(out, lse, ref, ref_lse, what="decode after a timed-out wait")
+    assert pkv.device_errors() == 0
+
+
 # ---- batch_classify_reorder ------------------------------------------------------------------
 
 def _reorder_case(R, seed, thr=1):

@@ -47,7 +47,8 @@ struct TcCfg {
   static constexpr int RING_OFF = 2 * TILE_BYTES;
   static constexpr int REQ_OFF = RING_OFF + NBUF * TILE_BYTES;  // int4 {r, row0, q_len, C}
   static constexpr int START_OFF = REQ_OFF + MAXR * 16;
-  static constexpr int BAR_OFF = START_OFF + (MAXR + 2) * 4;
+  static constexpr int PERM_OFF = START_OFF + (MAXR + 2) * 4;  // set positions by cost, heaviest first
+  static constexpr int BAR_OFF = PERM_OFF + MAXR * 4;
   // barriers: q_full, q_empty, kv_full[NBUF], kv_empty[NBUF], s_full[2], p_full[2], o_final[2]
   static constexpr int NBAR = 2 + 2 * NBUF + 6;
   static constexpr int SMEM = 1024 + BAR_OFF + NBAR * 8 + 16;
@@ -74,10 +75,11 @@ __device__ __forceinline__ void tc_resolve_set(const AttnParams& p, int& begin, 
   }
 }
 
-// Decode work item w (all roles walk the same sequence of items); s_req holds
-// {request id, first query row, q_len, cached tokens} of each request of the set.
+// Work item w (all roles walk the same sequence of items); s_req holds {request id, first
+// query row, q_len, cached tokens} of each request of the set, s_perm the set positions by
+// decreasing tile cost, s_start the prefix of q-tiles in that order.
 __device__ __forceinline__ TcItem tc_item(const AttnParams& p, const int* s_start, const int4* s_req,
-                                          int n, int64_t w, int HP) {
+                                          const int* s_perm, int n, int64_t w, int HP) {
   TcItem it;
   const int tg = static_cast<int>(w / HP), hp = static_cast<int>(w % HP);
   int lo = 0, hi = n - 1;
@@ -85,7 +87,7 @@ __device__ __forceinline__ TcItem tc_item(const AttnParams& p, const int* s_star
     const int mid = (lo + hi + 1) >> 1;
     if (s_start[mid] <= tg) lo = mid; else hi = mid - 1;
   }
-  const int4 q = s_req[lo];
+  const int4 q = s_req[s_perm[lo]];
   it.r = q.x;
   it.row0 = q.y;
   it.q_len = q.z;
@@ -100,6 +102,21 @@ __device__ __forceinline__ TcItem tc_item(const AttnParams& p, const int* s_star
   it.h0 = p.G >= 2 ? 2 * hp : hp;
   it.kh = it.h0 / p.G;
   return it;
+}
+
+// Key tiles a q-tile of a set request walks at most (its context plus its new tokens): the
+// schedule's cost of the request's items.
+__device__ __forceinline__ int tc_cost(const int4& q) { return (q.w + 127) / 128 + (q.z + 127) / 128; }
+
+// The items are in decreasing cost (requests by cost, their later q-tiles first) and are dealt
+// to the G CTAs in snake order (0..G-1, G-1..0, ...), so that every CTA's total stays close to
+// the mean: CTA c takes items c, 2G-1-c, 2G+c, 4G-1-c, ..., i.e. steps of 2(G-c)-1 and 2c+1 in
+// turn.
+__device__ __forceinline__ int64_t tc_next(int64_t w, int& odd) {
+  const int64_t step = odd ? 2 * static_cast<int64_t>(blockIdx.x) + 1
+                           : 2 * static_cast<int64_t>(gridDim.x - blockIdx.x) - 1;
+  odd ^= 1;
+  return w + step;
 }
 
 // Bounded wait that also gives up as soon as another role has given up.
@@ -138,6 +155,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
   uint8_t* sQ = smem;                  // [slot][half][128][128 B]
   uint8_t* ring = smem + C::RING_OFF;  // [NBUF][half][128][128 B]
   int* s_start = reinterpret_cast<int*>(smem + C::START_OFF);
+  int* s_perm = reinterpret_cast<int*>(smem + C::PERM_OFF);
   int4* s_req = reinterpret_cast<int4*>(smem + C::REQ_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
@@ -180,31 +198,43 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
   }
   if (warp == 9) tc::tmem_alloc(&s_tmem, 512);
 
-  // exclusive prefix of 128-row q-tiles per request of the set
+  // the set's requests
+  for (int i = tid; i < n; i += C::THREADS) {
+    const int r = p.order ? p.order[begin + i] : begin + i;
+    int4 q = make_int4(0, 0, 0, 0);
+    if (r >= 0 && r < p.batch_reqs) {
+      const int q_len = max(0, p.cu_q[r + 1] - p.cu_q[r]);
+      int Cc = 0;
+      if (p.seq_lens != nullptr) {
+        Cc = max(0, p.seq_lens[r] - q_len);
+        if (Cc > p.max_blocks * 16) {
+          if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_LEN);
+          Cc = p.max_blocks * 16;
+        }
+      }
+      q = make_int4(r, p.cu_q[r], q_len, Cc);
+    } else if (blockIdx.x == 0) {
+      flag_error(p.err, PKV_DEVERR_REQS);
+    }
+    s_req[i] = q;
+  }
+  __syncthreads();
+  // rank by cost, heaviest first, ties in set order (a stable order every CTA computes alike)
+  for (int i = tid; i < n; i += C::THREADS) {
+    const int ki = tc_cost(s_req[i]);
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const int kj = tc_cost(s_req[j]);
+      rank += (kj > ki || (kj == ki && j < i)) ? 1 : 0;
+    }
+    s_perm[rank] = i;
+  }
+  __syncthreads();
+  // exclusive prefix of 128-row q-tiles in that order
   int carry = 0;
   for (int base = 0; base < n; base += C::THREADS) {
-    const int i = base + tid;
-    int t = 0;
-    if (i < n) {
-      const int r = p.order ? p.order[begin + i] : begin + i;
-      int4 q = make_int4(0, 0, 0, 0);
-      if (r >= 0 && r < p.batch_reqs) {
-        const int q_len = max(0, p.cu_q[r + 1] - p.cu_q[r]);
-        int Cc = 0;
-        if (p.seq_lens != nullptr) {
-          Cc = max(0, p.seq_lens[r] - q_len);
-          if (Cc > p.max_blocks * 16) {
-            if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_LEN);
-            Cc = p.max_blocks * 16;
-          }
-        }
-        q = make_int4(r, p.cu_q[r], q_len, Cc);
-        t = (q_len + 127) / 128;
-      } else if (blockIdx.x == 0) {
-        flag_error(p.err, PKV_DEVERR_REQS);
-      }
-      s_req[i] = q;
-    }
+    const int j = base + tid;
+    const int t = j < n ? (s_req[s_perm[j]].z + 127) / 128 : 0;
     int x = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -218,7 +248,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
       if (w < warp) wprefix += s_scan[w];
       tot += s_scan[w];
     }
-    if (i < n) s_start[i] = carry + wprefix + x - t;
+    if (j < n) s_start[j] = carry + wprefix + x - t;
     carry += tot;
     __syncthreads();
   }
@@ -236,8 +266,9 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
     const int t = tid & 127;  // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t sc = 0, oc = 0;
-    for (int64_t w = blockIdx.x; w < W; w += gridDim.x) {
-      const TcItem it = tc_item(p, s_start, s_req, n, w, HP);
+    int odd = 0;
+    for (int64_t w = blockIdx.x; w < W; w = tc_next(w, odd)) {
+      const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (slot >= it.nslot) continue;
       const int qi = it.qr0 + t;  // query index of this row within its request
       float m = -CUDART_INF_F, l = 0.f;
@@ -386,8 +417,9 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
     }
     uint32_t kvc = 0, items = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < W && ok; w += gridDim.x, ++items) {
-      const TcItem it = tc_item(p, s_start, s_req, n, w, HP);
+    int odd = 0;
+    for (int64_t w = blockIdx.x; w < W && ok; w = tc_next(w, odd), ++items) {
+      const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (items > 0 && !tc_wait_warp(q_empty, (items - 1) & 1, &s_abort, p.err)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, it.nslot * C::TILE_BYTES);
@@ -455,8 +487,9 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         tc::mma_ts(tmem + ocol(slot), tmem + scol(slot) + k * 8,
                    tc::smem_desc(vb + k * 2048, C::HALF_BYTES, 1024), C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
     };
-    for (int64_t w = blockIdx.x; w < W && ok; w += gridDim.x, ++items) {
-      const TcItem it = tc_item(p, s_start, s_req, n, w, HP);
+    int odd = 0;
+    for (int64_t w = blockIdx.x; w < W && ok; w = tc_next(w, odd), ++items) {
+      const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       const bool two = it.nslot == 2;
       if (!tc_wait_warp(q_full, items & 1, &s_abort, p.err)) break;
       int prev_vbuf = -1;

@@ -61,6 +61,30 @@ def test_kv_cache_write_strided_cache_and_bad_slots(pkv):
     assert _errors(pkv) & 0x1
 
 
+@pytest.mark.parametrize("bs", [1, 8, 32, 64])
+def test_write_pack_unpack_other_block_sizes(pkv, bs):
+    """kv_cache_write, kv_block_pack and kv_block_unpack take any block size: bit for bit the
+    oracle's at 1, 8, 32 and 64 tokens per block (the attention calls take 16)."""
+    L = gen.write_pack_layers(1, 150, Hkv=2, D=64, block_size=bs, seed=70 + bs)[0]
+    gk, gv = L.k_cache.to(DEV), L.v_cache.to(DEV)
+    pkv.kv_cache_write(L.key.to(DEV), L.value.to(DEV), L.slot_mapping.to(DEV), gk, gv)
+    kc, vc = bits(L.k_cache).copy(), bits(L.v_cache).copy()
+    assert oracle.kv_cache_write(bits(L.key), bits(L.value), L.slot_mapping.numpy(), kc, vc) == 0
+    assert np.array_equal(bits(gk), kc) and np.array_equal(bits(gv), vc)
+    packed = pkv.kv_block_pack(gk, gv, L.block_ids.to(DEV))
+    exp, bad = oracle.kv_block_pack(kc, vc, L.block_ids.numpy())
+    assert bad == 0 and np.array_equal(bits(packed), exp)
+    # the prompt's rows come back in order from the blocks in table order
+    assert np.array_equal(exp[0].reshape(-1, 2, 64)[:150], bits(L.key))
+    rk, rv = torch.zeros_like(gk), torch.zeros_like(gv)
+    ids = torch.flip(L.block_ids, [0]).contiguous()
+    pkv.kv_block_unpack(packed, ids.to(DEV), rk, rv)
+    ek, ev = np.zeros_like(kc), np.zeros_like(vc)
+    assert oracle.kv_block_unpack(exp, ids.numpy(), ek, ev) == 0
+    assert np.array_equal(bits(rk), ek) and np.array_equal(bits(rv), ev)
+    assert _errors(pkv) == 0
+
+
 def test_kv_cache_write_empty(pkv):
     c = torch.zeros((2, 16, 1, 64), dtype=torch.bfloat16, device=DEV)
     e = torch.empty((0, 1, 64), dtype=torch.bfloat16, device=DEV)

@@ -401,11 +401,23 @@ def bench_mixed(pkv, dev, stream, timer, steps, warmup):
     n0 = pkv.launch_count()
     ms, sec = timer.run(step, steps, warmup)
     launches = (pkv.launch_count() - n0) // (warmup + 2 * steps)  # warm-up, timed and marked passes
+
+    # the unified variant for comparison: reorder-free, the whole batch in arrival order through
+    # one extend_attn call (decode = one new token, prefill = no cached tokens)
+    max_q, max_s = max(b.q_lens), max(b.seq_lens_list)
+
+    def unified(marks):
+        pkv.kv_cache_write(g.k_new, g.v_new, meta["slot_mapping"], g.k_cache, g.v_cache, stream=stream)
+        pkv.extend_attn(g.q, g.k_new, g.v_new, meta["cu_q"], meta["seq_lens"], g.k_cache, g.v_cache,
+                        meta["block_tables"], max_q, max_s, reqs=pkv.Reqs(R, R), chunk_budget_tokens=32768,
+                        scale=scale, out=out, lse=lse, stream=stream)
+
+    ums, _ = timer.run(unified, steps, warmup, sections=False)
     dec_bytes = sum(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.DECODE) * b.Hkv * b.D * 4
     ext_flops = sum(4 * b.Hq * b.D * (q * (s - q) + q * (q + 1) // 2)
                     for k, q, s in zip(kinds, b.q_lens, b.seq_lens_list) if k == gen.EXTEND)
     pre_flops = sum(4 * b.Hq * b.D * q * (q + 1) // 2 for k, q in zip(kinds, b.q_lens) if k == gen.PREFILL)
-    return dict(b=b, ms=ms, sec=sec, launches=launches, tokens=T, dec_bytes=dec_bytes,
+    return dict(b=b, ms=ms, sec=sec, launches=launches, tokens=T, dec_bytes=dec_bytes, unified_ms=ums,
                 ext_flops=ext_flops, pre_flops=pre_flops)
 
 
@@ -656,6 +668,10 @@ def main():
                              (peaks["bf16_sust"] * 1e12)) * 1e3,
             }
             extras["mixed_batch"]["frac_of_bound"] = extras["mixed_batch"]["bound_ms"] / mms
+            ums = sum(m["unified_ms"]) / len(m["unified_ms"])
+            extras["mixed_batch"]["unified_single_call"] = {
+                "what": "write + one extend_attn over all requests in arrival order (no reorder, no routing)",
+                "ms_per_step": ums, "tokens_per_s": m["tokens"] / (ums * 1e-3)}
             del m
         except Exception as e:  # report, keep the headline
             extras["mixed_batch"] = {"error": repr(e)}

@@ -448,6 +448,32 @@ def test_mixed_batch_pipeline(pkv, D):
     compare_attention(out, lse, ref, ref_lse, rows=np.ones(T, bool), what=f"mixed D={D}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_mixed_batch_unified_single_call(pkv, D):
+    """The unified variant (vLLM blog "rocm-attention-backend", "Unified attention backends":
+    one kernel for every token type): the whole batch in arrival order through one extend_attn
+    call — decode requests are extend requests with one new token, prefill requests extend
+    requests with no cached tokens. Same results as the three routed calls, against the oracle."""
+    b = gen.mixed_batch(20, (10, 400), 3, 70, (30, 300), 3, (10, 150), Hq=16, Hkv=2, D=D, seed=33 + D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    R, T = b.R, b.T
+    pkv.kv_cache_write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    out, lse = pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, g.k_cache, g.v_cache, g.block_tables,
+                               max(b.q_lens), max(b.seq_lens_list), scale=scale)
+    assert _errors(pkv) == 0
+    kc, vc = bits(b.k_cache).copy(), bits(b.v_cache).copy()
+    oracle.kv_cache_write(bits(b.k_new), bits(b.v_new), b.slot_mapping.numpy(), kc, vc)
+    e_perm, e_b, _, _ = oracle.batch_classify_reorder(b.cu_q.numpy(), b.seq_lens.numpy())
+    ref = np.full((T, b.Hq, D), np.nan)
+    ref_lse = np.full((T, b.Hq), np.nan)
+    oracle_decode(b, kc, vc, scale, req_ids=e_perm[e_b[0]:e_b[1]], out=ref, lse=ref_lse)
+    oracle_extend(b, kc, vc, scale, req_ids=e_perm[e_b[1]:e_b[2]], out=ref, lse=ref_lse)
+    oracle_prefill(b, scale, req_ids=e_perm[e_b[2]:e_b[3]], out=ref, lse=ref_lse)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, rows=np.ones(T, bool), what=f"unified D={D}")
+
+
 def test_request_set_cut_to_max_reqs_is_flagged(pkv):
     b = gen.decode_batch(6, 10, 60, Hq=4, Hkv=1, D=64, seed=2)
     g = b.to(DEV)

@@ -70,6 +70,8 @@ def _load():
             lib.oracle_paged_decode_fp8.argtypes = [P, P, P, i64, i32, i32, i32, P, i32, P, P, P,
                                                     i32, i32, f64, f64, f64, P, P, i32]
             lib.oracle_paged_decode_fp8.restype = None
+            lib.oracle_mla_decode.argtypes = [P, P, i64, i32, i32, i32, P, i32, P, P, P, i32, i32, f64, P, P, i32]
+            lib.oracle_mla_decode.restype = None
             lib.oracle_extend.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, P, i32, i32,
                                           i32, i32, f64, P, P, P, i32]
             lib.oracle_extend.restype = None
@@ -199,6 +201,30 @@ def paged_decode_fp8(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale
                                 block_tables.shape[1], _ptr(seq_lens), _ptr(cu_q), _ptr(req_ids), n_req, Hq,
                                 float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
                                 nthreads or default_threads())
+    return out, lse
+
+
+def mla_decode(q, cache, block_tables, seq_lens, scale, v_dim, cu_q=None, req_ids=None, n_req=None,
+               nthreads=None, out=None, lse=None):
+    """Absorbed MLA decode: q [T, Hq, Dk] bits, latent cache [nb, bs, 1, Dk] bits (keys = all
+    Dk dims, values = the first v_dim). Returns (out [T, Hq, v_dim], lse [T, Hq]) float64."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    cache = _c(cache, np.uint16)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    cu_q, req_ids = _c(cu_q, np.int32), _c(req_ids, np.int32)
+    T, Hq, Dk = q.shape
+    nb, bs = cache.shape[:2]
+    assert int(np.prod(cache.shape[2:])) == Dk
+    if n_req is None:
+        n_req = req_ids.shape[0] if req_ids is not None else seq_lens.shape[0]
+    if out is None:
+        out = np.full((T, Hq, v_dim), np.nan)
+    if lse is None:
+        lse = np.full((T, Hq), np.nan)
+    lib.oracle_mla_decode(_ptr(q), _ptr(cache), nb, bs, Dk, int(v_dim), _ptr(block_tables), block_tables.shape[1],
+                          _ptr(seq_lens), _ptr(cu_q), _ptr(req_ids), n_req, Hq, float(scale), _ptr(out), _ptr(lse),
+                          nthreads or default_threads())
     return out, lse
 
 

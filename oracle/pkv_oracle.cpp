@@ -146,6 +146,35 @@ inline uint8_t e4m3_encode(float x) {
   return sign | static_cast<uint8_t>(best);
 }
 
+// attend_row with keys of Dk dims and values of Dv dims (separate arrays [n][Dk], [n][Dv]).
+void attend_row_kv(const double* q, const double* keys, const double* vals, int64_t n, int Dk, int Dv,
+                   double scale, double* o, double* lse) {
+  if (n <= 0) {
+    for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+    *lse = -std::numeric_limits<double>::infinity();
+    return;
+  }
+  std::vector<double> s(static_cast<size_t>(n));
+  double m = -std::numeric_limits<double>::infinity();
+  for (int64_t j = 0; j < n; ++j) {
+    double acc = 0.0;
+    for (int d = 0; d < Dk; ++d) acc += q[d] * keys[j * Dk + d];
+    s[j] = scale * acc;
+    if (s[j] > m) m = s[j];
+  }
+  double z = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    s[j] = std::exp(s[j] - m);
+    z += s[j];
+  }
+  for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    const double w = s[j] / z;
+    for (int d = 0; d < Dv; ++d) o[d] += w * vals[j * Dv + d];
+  }
+  *lse = m + std::log(z);
+}
+
 struct Paged {
   const uint16_t* k_cache;
   const uint16_t* v_cache;
@@ -531,6 +560,36 @@ void oracle_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const ui
       for (int d = 0; d < D; ++d) qd[d] = bf16_value(q[(row * Hq + h) * D + d]);
       attend_row(qd.data(), K.data(), V.data(), n, D, scale, out + (row * Hq + h) * D,
                  lse + row * Hq + h);
+    }
+  });
+}
+
+// ---- MLA absorbed decode ---------------------------------------------------------------
+// [ROCm-attn] "AITER MLA backend": DeepSeek-style MLA keeps one compressed 576-dim latent per
+// token in the KV cache; decode works directly in that latent space ("absorbed"): every query
+// head attends over the latent rows as keys (all Dk dims) and takes the first Dv dims of the
+// same rows as values. Cache [num_blocks][bs][Dk] (one latent "head"); q [T][Hq][Dk];
+// out [T][Hq][Dv], lse [T][Hq].
+void oracle_mla_decode(const uint16_t* q, const uint16_t* cache, int64_t num_blocks, int32_t bs, int32_t Dk,
+                       int32_t Dv, const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                       const int32_t* cu_q, const int32_t* req_ids, int32_t n_req, int32_t Hq, double scale,
+                       double* out, double* lse, int32_t nthreads) {
+  const Paged P{cache, cache, num_blocks, bs, 1, Dk, block_tables, max_blocks};
+  parallel_for(static_cast<int64_t>(n_req), nthreads, [&](int64_t item) {
+    const int64_t r = req_ids ? req_ids[item] : item;
+    const int64_t row = cu_q ? cu_q[r] : r;
+    const int64_t n = seq_lens[r];
+    const size_t nn = static_cast<size_t>(std::max<int64_t>(n, 0));
+    std::vector<double> K(nn * Dk), V(nn * Dv), qd(Dk);
+    for (int64_t j = 0; j < n; ++j) {
+      const int64_t off = paged_offset(P, r, j, 0);
+      for (int d = 0; d < Dk; ++d) K[j * Dk + d] = off < 0 ? NAN : bf16_value(cache[off + d]);
+      for (int d = 0; d < Dv; ++d) V[j * Dv + d] = off < 0 ? NAN : bf16_value(cache[off + d]);
+    }
+    for (int h = 0; h < Hq; ++h) {
+      for (int d = 0; d < Dk; ++d) qd[d] = bf16_value(q[(row * Hq + h) * Dk + d]);
+      attend_row_kv(qd.data(), K.data(), V.data(), n, Dk, Dv, scale, out + (row * Hq + h) * Dv,
+                    lse + row * Hq + h);
     }
   });
 }

@@ -539,3 +539,33 @@ def test_fp8_decode_matches_torch_sdpa_on_dequantised_cache():
         exp = sdpa(qf[r:r + 1], k, v, scale)[0]
         assert np.abs(out[r] - exp).max() < TOL
         assert np.abs(lse[r] - lse_ref(qf[r:r + 1], k, scale)[0]).max() < TOL
+
+
+# ---- MLA absorbed decode ----------------------------------------------------------------------------
+
+def test_mla_decode_matches_torch_sdpa_with_latent_values():
+    """Absorbed MLA decode == SDPA in fp64 with keys = the latent rows (all Dk dims) and values =
+    their first Dv dims, every query head against the one latent head."""
+    Dk, Dv, Hq = 40, 32, 8
+    b = gen.decode_batch(3, 5, 70, Hq=Hq, Hkv=1, D=Dk, seed=80)
+    scale = 0.11
+    out, lse = oracle.mla_decode(gen.bf16_bits(b.q), gen.bf16_bits(b.k_cache), b.block_tables.numpy(),
+                                 b.seq_lens.numpy(), scale, Dv)
+    qf = f64(gen.bf16_bits(b.q))
+    for r in range(b.R):
+        k, _ = dense_kv(b, r, b.seq_lens_list[r])          # [n, 1, Dk] latent rows
+        v = k[:, :, :Dv].contiguous()
+        exp = sdpa(qf[r:r + 1], k, v, scale)[0]
+        assert np.abs(out[r] - exp).max() < TOL
+        assert np.abs(lse[r] - lse_ref(qf[r:r + 1], k, scale)[0]).max() < TOL
+
+
+def test_mla_decode_with_full_values_is_the_one_kv_head_decode():
+    """With Dv = Dk the latent is both key and value: the generic decode with one KV head
+    (whose V cache is the same latent) gives the same result."""
+    D = 24
+    b = gen.decode_batch(4, 1, 90, Hq=4, Hkv=1, D=D, seed=81)
+    lat = gen.bf16_bits(b.k_cache)
+    out, lse = oracle.mla_decode(gen.bf16_bits(b.q), lat, b.block_tables.numpy(), b.seq_lens.numpy(), 0.2, D)
+    ref, ref_lse = oracle.paged_decode(gen.bf16_bits(b.q), lat, lat, b.block_tables.numpy(), b.seq_lens.numpy(), 0.2)
+    assert np.abs(out - ref).max() < 1e-12 and np.abs(lse - ref_lse).max() < 1e-12

@@ -292,6 +292,40 @@ def bench_decode_fp8(pkv, dev, stream, timer, steps, warmup):
     return dict(step_ms=step_ms, launch_ms=dec_ms, kv_bytes=kv_bytes, alg_bytes=kv_bytes + other, R=R)
 
 
+def bench_mla(pkv, dev, stream, timer, steps, warmup):
+    """Absorbed MLA decode, DeepSeek-R1-like layer under tensor parallelism 8 (16 query heads
+    over a 576-wide latent, 128 requests at 10K-11K tokens). Step = kv_cache_write of the new
+    tokens' latent rows + mla_decode_attn."""
+    b = gen.mla_batch(**gen.MLA_DEEPSEEK_TP8, device=dev)
+    R, maxs = b.R, max(b.seq_lens_list)
+    bt64 = b.block_tables.to(torch.int64)
+    pos = (b.seq_lens.to(torch.int64) - 1)
+    slots = bt64[torch.arange(R, device=dev), pos // 16] * 16 + pos % 16
+    new_rows = gen.randn_bf16((R, 1, gen.MLA_DEEPSEEK_TP8["Dk"]), torch.Generator(device=dev).manual_seed(7), dev)
+    out = torch.empty((R, b.Hq, gen.MLA_DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, b.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, pkv.mla_decode_workspace_size(R, b.Hq, maxs)), dtype=torch.uint8, device=dev)
+    lat_bytes = sum(b.seq_lens_list) * b.Dk * 2
+    other = b.q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + sum((x + 15) // 16 for x in b.seq_lens_list) * 4
+
+    def decode():
+        pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, maxs, gen.MLA_SCALE, out=out, lse=lse,
+                            workspace=ws, stream=stream)
+
+    def step(marks):
+        pkv.kv_cache_write(new_rows, new_rows, slots, b.latent, b.latent, stream=stream)
+        decode()
+
+    ms, _ = timer.run(step, steps, warmup, sections=False)
+    launch_ms, _ = timer.run(lambda m: decode(), max(steps, 20), warmup, sections=False)
+    errs = pkv.device_errors(clear=True)
+    step_ms = sum(ms) / len(ms)
+    dec_ms = sum(launch_ms) / len(launch_ms)
+    flops = 2.0 * sum(b.seq_lens_list) * b.Hq * (b.Dk + gen.MLA_DV)
+    return dict(step_ms=step_ms, launch_ms=dec_ms, lat_bytes=lat_bytes, alg_bytes=lat_bytes + other, R=R,
+                flops=flops, errors=errs)
+
+
 def bench_decode_e2e(pkv, w, dev, stream, steps, warmup, timer):
     """The same step through the public API with host buffers: every input of the step (q, the
     new K/V, slot mapping, lengths, block tables) is copied from pinned host memory and out/lse
@@ -533,6 +567,14 @@ def profile_case(pkv, args):
         fn = lambda: pkv.paged_decode_attn(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, maxs,
                                            cu_q=b.cu_q, workspace=ws)
         what = f"decode B=64 kv_bytes={sum(b.seq_lens_list) * 4 * 128 * 4}"
+    elif args.profile == "mla":
+        # 32 requests of the MLA workload's shape: ~390 MB of latent rows per launch
+        b = gen.mla_batch(32, 10000, 11000, Hq=16, seed=5, device=dev)
+        maxs = max(b.seq_lens_list)
+        ws = torch.empty(max(16, pkv.mla_decode_workspace_size(b.R, 16, maxs)), dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, maxs, gen.MLA_SCALE,
+                                         workspace=ws)
+        what = f"mla B=32 latent_bytes={sum(b.seq_lens_list) * 1152}"
     elif args.profile == "prefill":
         b = gen.prefill_batch([4096, 4096], Hq=64, Hkv=8, D=128, seed=5, device=dev)
         fn = lambda: pkv.varlen_prefill_attn(b.q, b.k_new, b.v_new, b.cu_q, 4096)
@@ -565,7 +607,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["decode", "prefill", "extend", "write_pack"], default=None,
+    ap.add_argument("--profile", choices=["decode", "mla", "prefill", "extend", "write_pack"], default=None,
                     help="run a reduced case of one kernel --steps times for an ncu capture; prints "
                          "a one-line summary, no benchmark line")
     args = ap.parse_args()
@@ -691,6 +733,23 @@ def main():
             }
         except Exception as e:
             extras["decode_fp8"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            r = bench_mla(pkv, dev, stream, timer, steps, warmup)
+            extras["mla_decode"] = {
+                "workload": "DeepSeek-R1-like MLA layer, tensor parallel 8: 128 seqs, ctx U[10000,11000], "
+                            "Hq 16 over one 576-wide latent (values = first 512 dims), block 16; step = "
+                            "kv_cache_write of the new latent rows + mla_decode_attn",
+                "latent_bytes_per_step": r["lat_bytes"], "ms_per_step": r["step_ms"],
+                "latent_gbs": r["lat_bytes"] / (r["step_ms"] * 1e-3) / 1e9,
+                "decode_tokens_per_s": r["R"] / (r["step_ms"] * 1e-3),
+                "launch_ms": r["launch_ms"],
+                "roofline_frac": r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"],
+                "mma_tflops": r["flops"] / (r["launch_ms"] * 1e-3) / 1e12,
+                "device_errors": r["errors"],
+            }
+        except Exception as e:
+            extras["mla_decode"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         for kind in ("prefill", "extend_long"):
             try:

@@ -59,7 +59,9 @@
  *
  * Supported shapes (anything else returns PKV_ERR_UNSUPPORTED; there is no fallback path):
  *   head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}; block_size 16 for the
- *   attention calls (kv_cache_write and kv_block_pack take any block_size >= 1).
+ *   attention calls (kv_cache_write and kv_block_pack take any block_size >= 1). The MLA
+ *   decode takes one 576-wide latent head, 512 value dims and 16 to 128 query heads in
+ *   groups of 16.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -216,6 +218,31 @@ pkv_status pkv_paged_decode_attn_noalloc(const void* q, pkv_cache cache,
                                          const int32_t* seq_lens, const int32_t* cu_q,
                                          pkv_reqs reqs, int32_t num_q_heads, int32_t max_seq_len,
                                          float scale, void* out, float* lse, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * mla_decode_attn — absorbed MLA decode over a paged latent cache.
+ * Source: vLLM blog "rocm-attention-backend", section "AITER MLA backend" (DeepSeek-style MLA
+ * caches one 576-wide compressed latent row per token; decode is "absorbed": it works
+ * directly in that latent space) and its MLA benchmark (DeepSeek-R1, tensor parallel 8,
+ * block_size 16).
+ * The cache holds the latent rows: cache.k = bf16 [num_blocks, 16, 1, 576] (num_kv_heads 1,
+ * head_dim 576, block_size 16, kv_dtype PKV_KV_BF16; cache.v is not read and may equal
+ * cache.k). For each request r of `reqs` (q_len 1; query row cu_q[r], or r when cu_q is
+ * NULL), each query head h, with c_j = the latent row of position j < seq_lens[r]:
+ *   out[row, h] = sum_j softmax_j(scale * q[row, h] . c_j) * c_j[0 .. v_dim-1]   (bf16),
+ *   lse[row, h] = ln sum_j exp(scale * q[row, h] . c_j)                          (fp32).
+ * q: bf16 [rows, num_q_heads, 576]; out: bf16 [rows, num_q_heads, v_dim]; v_dim must be 512
+ * and num_q_heads a multiple of 16 (at most 128). Lengths, the error word and the workspace
+ * behave as in paged_decode_attn; the workspace size comes from
+ * pkv_mla_decode_workspace_size with the same num_q_heads. Other shapes return
+ * PKV_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------------------- */
+size_t pkv_mla_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int32_t max_seq_len);
+pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_q,
+                               pkv_reqs reqs, int32_t num_q_heads, int32_t max_seq_len,
+                               float scale, int32_t v_dim, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * extend_attn — new tokens against their cached context plus themselves (causal).

@@ -207,6 +207,36 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, seq_lens, max_s
     return out, lse
 
 
+def mla_decode_attn(q, latent_cache, block_tables, seq_lens, max_seq_len, scale, v_dim=512, cu_q=None,
+                    reqs: Optional[Reqs] = None, out=None, lse=None, workspace=None, stream=None):
+    """Absorbed MLA decode. q [T, Hq, 576]; latent_cache [num_blocks, 16, 1, 576] bf16 (keys =
+    all 576 dims of a token's latent row, values = its first v_dim). Returns out [T, Hq, v_dim]
+    and lse [T, Hq]. The softmax scale is the model's (no default)."""
+    lib = _lib.load()
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    cache = make_cache(latent_cache, latent_cache)
+    T, Hq, Dk = q.shape
+    R = seq_lens.numel()
+    reqs = reqs or Reqs(max_reqs=R, batch_reqs=R)
+    if out is None:
+        out = torch.empty((T, Hq, v_dim), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    need = lib.pkv_mla_decode_workspace_size(reqs.max_reqs, Hq, max_seq_len)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_mla_decode_attn(_ptr(q), cache, _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                   _ptr(cu_q), reqs.c(), Hq, max_seq_len, float(scale), int(v_dim), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), need, _stream(stream)), "mla_decode_attn")
+    return out, lse
+
+
+def mla_decode_workspace_size(max_reqs, num_q_heads, max_seq_len) -> int:
+    return int(_lib.load().pkv_mla_decode_workspace_size(max_reqs, num_q_heads, max_seq_len))
+
+
 def extend_attn(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, max_q_len,
                 max_seq_len, reqs: Optional[Reqs] = None, chunk_budget_tokens=32768, scale=None,
                 out=None, lse=None, stream=None):

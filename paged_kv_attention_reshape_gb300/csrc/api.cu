@@ -361,6 +361,8 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   p.Hq = num_q_heads;
   p.Hkv = cache.num_kv_heads;
   p.G = num_q_heads / cache.num_kv_heads;
+  p.units = p.Hkv;
+  p.out_dim = cache.head_dim;
   p.num_blocks = cache.num_blocks;
   p.max_seq_len = max_seq_len;
   const bool fp8 = cache.kv_dtype == PKV_KV_FP8_E4M3;
@@ -379,6 +381,69 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   int launches = 0;
   st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim, fp8,
                                        reinterpret_cast<cudaStream_t>(stream), &launches));
+  t_launches += launches;
+  return st;
+}
+
+size_t pkv_mla_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int32_t max_seq_len) {
+  (void)max_reqs;
+  (void)max_seq_len;
+  if (num_q_heads <= 0 || num_q_heads % 16 != 0 || num_q_heads > 128) return 0;
+  return mla_workspace_bytes(num_q_heads);
+}
+
+pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_q,
+                               pkv_reqs reqs, int32_t num_q_heads, int32_t max_seq_len, float scale,
+                               int32_t v_dim, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, pkv_stream_t stream) {
+  if (cache.v == nullptr) cache.v = cache.k;  // values are the leading dims of the same rows
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if ((st = check_reqs(reqs)) != PKV_OK) return st;
+  if (cache.kv_dtype != PKV_KV_BF16 || cache.num_kv_heads != 1 || cache.head_dim != 576 ||
+      cache.block_size != 16 || v_dim != 512)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads <= 0 || num_q_heads % 16 != 0 || num_q_heads > 128) return PKV_ERR_UNSUPPORTED;
+  if (max_blocks <= 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs == 0) return PKV_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs > 65535) return PKV_ERR_UNSUPPORTED;
+  DecodeParams p{};
+  p.err = error_word();
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.block_tables = block_tables;
+  p.max_blocks = max_blocks;
+  p.seq_lens = seq_lens;
+  p.cu_q = cu_q;
+  p.order = reqs.order;
+  p.bounds = reqs.bounds;
+  p.cls = reqs.cls;
+  p.max_reqs = reqs.max_reqs;
+  p.batch_reqs = reqs.batch_reqs;
+  p.Hq = num_q_heads;
+  p.Hkv = 1;
+  p.G = 16;                            // query heads per group
+  p.units = num_q_heads / 16 * 4;      // four 128-wide value slices per group
+  p.out_dim = v_dim;
+  p.num_blocks = cache.num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.v_scale = 1.f;
+  const size_t need = mla_workspace_bytes(num_q_heads);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  p.ws_part = static_cast<float*>(workspace);
+  p.ws_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                   mla_workspace_ctr_offset(num_q_heads));
+  p.epoch = next_epoch();
+  CUtensorMap tm;
+  if (!encode_cache(&tm, cache.k, cache)) return PKV_ERR_CUDA;
+  int launches = 0;
+  st = cuda_status(launch_mla_decode(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches));
   t_launches += launches;
   return st;
 }

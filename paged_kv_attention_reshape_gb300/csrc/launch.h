@@ -30,9 +30,13 @@ struct DecodeParams {
   int32_t max_seq_len;
   float scale_log2;      // softmax scale * log2(e) (times the key scale for an FP8 cache)
   float v_scale;         // FP8 cache: value of a V code = e4m3(code) * v_scale; 1 for bf16
-  float* ws_part;        // [shares][2][Hkv][G][D + 4] partials of sequences cut at share edges
-  unsigned long long* ws_ctr;  // [shares][Hkv] arrival counters of cut sequences: epoch << 32 | count
+  float* ws_part;        // [shares][2][units][G][D + 4] partials of sequences cut at share edges
+  unsigned long long* ws_ctr;  // [shares][units] arrival counters of cut sequences: epoch << 32 | count
   uint32_t epoch;        // distinct per call: counters left by earlier calls read as empty
+  // Work units of a share: one per KV head for decode (units = Hkv, out_dim = head_dim); for
+  // the MLA decode one per slice of the value dims of a group of G query heads (out_dim = the
+  // value width).
+  int32_t units, out_dim;
 };
 
 // Extend and prefill share one kernel; prefill is the case without cached context.
@@ -83,6 +87,7 @@ enum AttrSlot {
   kAttrDecode128Fp8,
   kAttrAttn64,
   kAttrAttn128,
+  kAttrMla,
   kAttrCount
 };
 
@@ -108,6 +113,10 @@ cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, co
 int decode_smem_bytes(int D);
 size_t decode_workspace_bytes(int Hq, int Hkv, int D);
 size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D);
+// Absorbed MLA decode: tm over the latent cache (one 576-wide head, bf16).
+cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, int* launches);
+size_t mla_workspace_bytes(int Hq);
+size_t mla_workspace_ctr_offset(int Hq);
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
 // (ignored for prefill).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -1,0 +1,478 @@
+// mla_decode.cu — absorbed MLA decode: every query head of a sequence against its paged
+// latent cache.
+//
+// vLLM blog "rocm-attention-backend", section "AITER MLA backend": DeepSeek-style MLA keeps
+// one compressed 576-wide latent row per token in the KV cache, and decode runs directly in
+// that latent space ("absorbed"): each query head scores all 576 dims of the latent rows and
+// takes the first 512 dims of the same rows as its values. The section's benchmark runs
+// DeepSeek-R1 with tensor parallelism 8 and block size 16, i.e. 16 query heads per GPU
+// sharing one latent row per token.
+//
+// Design (HBM-bound at 16 heads per group: 2 x 16 x 1088 flops per 1152-byte row):
+//   * the work split is the decode call's: the set's 16-token blocks in equal contiguous
+//     shares of a fixed grid, cut sequences merged in-kernel by the last arriving piece;
+//   * a CTA serves one share for one group of 16 query heads: four compute warps and one
+//     producer warp. The producer walks the share and streams whole blocks (16 rows x 576
+//     dims = 18 KB, nine 64-wide TMA boxes with the 128-byte swizzle) into a ring of NS
+//     stages; a stage is refilled once the four compute warps have arrived on its "empty"
+//     barrier;
+//   * the piece's query slice of a warp (16 heads x 144 dims) is fetched with cp.async when
+//     the previous piece ends, and its MMA fragments are re-read from shared memory for each
+//     block (registers go to the 16 x 128 fp32 output accumulator);
+//   * the 16 heads sit on the M dimension of the warp-level bf16 MMA (m16n8k16, fp32
+//     accumulate). Compute warp w scores dims 144w .. 144w + 143 (its query slice stays in
+//     registers), the four partial 16 x 16 score tiles are summed through shared memory
+//     behind one named barrier (in the same order by every warp, so all four hold identical
+//     scores and softmax state), and warp w accumulates output dims 128w .. 128w + 127;
+//   * each warp is one "unit" of the split-KV merge (a 128-wide slice of a 16-head group):
+//     a piece cut at a share edge stores its slice's partial and arrives on its own counter.
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "decode_shares.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+struct MlaCfg {
+  static constexpr int DK = 576;                 // latent row: scored dims
+  static constexpr int DV = 512;                 // leading dims that are the values
+  static constexpr int BS = 16;                  // tokens per block
+  static constexpr int HG = 16;                  // query heads per CTA (the MMA's M)
+  static constexpr int NCW = 4;                  // compute warps
+  static constexpr int THREADS = (NCW + 1) * 32; // + the producer warp
+  static constexpr int KW = DK / NCW;            // 144 scored dims per warp
+  static constexpr int KSW = KW / 16;            // 9 k-steps per warp
+  static constexpr int VW = DV / NCW;            // 128 output dims per warp
+  static constexpr int BOXES = DK / 64;          // 9 TMA boxes per block
+  static constexpr int STAGE_BYTES = BOXES * BS * 128;  // 18432
+  static constexpr int NS = 3;                   // ring stages (two CTAs fit on an SM)
+  static constexpr int Q_ROW = KW * 2 + 16;      // 304: a query slice row, padded off the banks
+  static constexpr int Q_BYTES = HG * Q_ROW;     // per compute warp
+  static constexpr int XCHG_BYTES = 2 * NCW * 32 * 8 * 4;  // two buffers of partial scores
+  static constexpr int MAXR = 1024;              // requests per set handled on device
+  static constexpr int MIN_BLOCKS = 8;           // smallest share a CTA is given
+  static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;
+  static constexpr int OFF_Q = NS * STAGE_BYTES;
+  static constexpr int OFF_X = OFF_Q + NCW * Q_BYTES;
+  static constexpr int OFF_TAB = OFF_X + XCHG_BYTES;
+  static constexpr int OFF_BAR = OFF_TAB + TAB_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 2 * NS * 8;
+};
+static_assert(MlaCfg::STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle");
+static_assert(MlaCfg::OFF_BAR % 8 == 0, "mbarrier alignment");
+
+// Named barrier 1 among the compute warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void compute_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(MlaCfg::NCW * 32) : "memory");
+}
+
+__global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const DecodeParams p,
+                                                                         const __grid_constant__ CUtensorMap tm) {
+  using C = MlaCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int* s_pre = reinterpret_cast<int*>(smem + C::OFF_TAB);
+  int* s_ctx = s_pre + C::MAXR + 1;
+  int* s_r = s_ctx + C::MAXR;
+  int* s_row = s_r + C::MAXR;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::NS;
+  __shared__ int s_scan[C::NCW + 1];
+  __shared__ int s_gave_up[2][C::NCW];  // per block (two buffers): compute warp w gave up waiting
+  __shared__ int s_abort;               // the compute warps stopped: the producer stops too
+  __shared__ uint32_t s_issued, s_used;
+
+  pdl_wait();
+  pdl_release();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_abort = 0;
+    s_issued = s_used = 0;
+  }
+
+  // ---- the set's sequences and their block counts (every CTA, redundantly) ----
+  int begin, n;
+  resolve_set(p, begin, n);
+  const int64_t TB = load_set<C::MAXR, C::BS>(p, begin, n, s_pre, s_ctx, s_r, s_row, s_scan);
+  if (TB == 0) return;
+
+  // ---- this CTA's share [b0, b1) of the blocks; its head group hg ----
+  const int nsh = active_shares(TB, gridDim.x, C::MIN_BLOCKS);
+  const Shares sh(TB, nsh);
+  const int c = blockIdx.x, hg = blockIdx.y;
+  if (c >= nsh) return;  // CTA-uniform
+  const int64_t b0 = sh.start(c), b1 = sh.start(c + 1);
+  if (b0 >= b1) return;
+  if (tid == 0) {
+    for (int st = 0; st < C::NS; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], C::NCW);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tm);
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ================= producer: walks the share and streams whole blocks =================
+    PieceIter lit;
+    lit.start(s_pre, n, 1, b0, b1);
+    Piece lpc{0, 0, 0, 0};
+    int lj = 0;                 // next block (local index) of lpc to load
+    bool lhave = false;         // lpc valid
+    int lbatch = 0, lnext = 0;  // this lane's table entries: block lpc.lo + lbase + lane (and +32)
+    int lfirst = 0;             // entry `lane` of the piece after lpc, loaded one piece early
+    int lbase = 0;
+    const int32_t* ltable = nullptr;
+    uint32_t issued = 0;
+    auto table_of = [&](const Piece& q) {
+      return p.block_tables + static_cast<int64_t>(s_r[q.i]) * p.max_blocks + q.lo;
+    };
+    for (;;) {
+      if (!lhave || lj == lpc.hi - lpc.lo) {  // next piece: its table entries, 32 per load
+        const bool first = !lhave;
+        if (!lit.next(lpc)) break;
+        lhave = true;
+        lj = 0;
+        lbase = 0;
+        ltable = table_of(lpc);
+        const int nb = lpc.hi - lpc.lo;
+        lbatch = first ? ((lane < nb) ? ltable[lane] : 0) : lfirst;
+        lnext = (32 + lane < nb) ? ltable[32 + lane] : 0;
+        PieceIter nx = lit;
+        Piece q;
+        lfirst = 0;
+        if (nx.next(q) && lane < q.hi - q.lo) lfirst = table_of(q)[lane];
+      } else if (lj == lbase + 32) {
+        lbase += 32;
+        lbatch = lnext;
+        lnext = (lbase + 32 + lane < lpc.hi - lpc.lo) ? ltable[lbase + 32 + lane] : 0;
+      }
+      int blk = __shfl_sync(0xffffffffu, lbatch, lj - lbase);
+      if (blk < 0 || blk >= p.num_blocks) {
+        if (lane == 0) flag_error(p.err, PKV_DEVERR_BLOCK);
+        blk = 0;
+      }
+      const int s = issued % C::NS;
+      if (issued >= C::NS) {
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ((issued / C::NS) - 1) & 1, p.err))) break;
+      }
+      if (lane == 0) {
+        uint8_t* dst = smem + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+#pragma unroll
+        for (int b = 0; b < C::BOXES; ++b) tma_load_4d(dst + b * (C::BS * 128), &tm, &full[s], 0, b, 0, blk);
+      }
+      ++lj;
+      ++issued;
+    }
+    if (lane == 0) s_issued = issued;
+  } else {
+    // ============ compute warp w: score dims 144w.., output dims 128w.. of 16 heads ============
+    const int w = warp;
+    const int unit = hg * C::NCW + w;  // this warp's unit of the split-KV merge
+    const int G = C::HG;
+    uint8_t* sQ = smem + C::OFF_Q + w * C::Q_BYTES;
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_X);
+
+    // query slice of a row: heads hg*16 .. +15, dims 144w .. 144w + 143, rows padded to 304 B
+    // (ldmatrix rows of a phase then fall on distinct banks)
+    auto request_q = [&](int64_t row) {
+      for (int c16 = lane; c16 < C::HG * (C::KW / 8); c16 += 32) {
+        const int gg = c16 / (C::KW / 8), chunk = c16 % (C::KW / 8);
+        const __nv_bfloat16* src = p.q + (row * p.Hq + hg * C::HG + gg) * C::DK + w * C::KW + chunk * 8;
+        cp_async16(sQ + gg * C::Q_ROW + chunk * 16, src, 16u);
+      }
+      cp_async_commit();
+    };
+
+    PieceIter cit;
+    cit.start(s_pre, n, 1, b0, b1);
+    {
+      PieceIter nx = cit;
+      Piece first;
+      if (nx.next(first)) request_q(s_row[first.i]);
+    }
+
+    // ---- deferred arrival of the last stored partial (as in the decode kernel) ----
+    bool pend = false;
+    unsigned long long* pend_ctr = nullptr;
+    unsigned long long pend_cur = 0;
+    int pend_np = 0, pend_c0 = 0, pend_c1 = 0;
+    int64_t pend_row = 0;
+    int due = 0;
+    int due_c0[2] = {0, 0}, due_c1[2] = {0, 0};
+    int64_t due_row[2] = {0, 0};
+    auto flush_arrival = [&]() {
+      __threadfence();
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) arrived = arrive_counter(pend_ctr, p.epoch, pend_np, pend_cur, p.err);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      pend = false;
+      if (arrived == pend_np) {
+        if (due < 2) {
+          due_c0[due] = pend_c0;
+          due_c1[due] = pend_c1;
+          due_row[due] = pend_row;
+          ++due;
+        } else if (lane == 0) {
+          flag_error(p.err, PKV_DEVERR_REQS);  // cannot happen: a share stores at most two partials
+        }
+      }
+    };
+
+    Piece pc;
+    uint32_t t = 0;  // blocks consumed
+    bool ok = true;
+    const int r0 = lane >> 2;  // fragment rows r0 and r0 + 8
+    while (ok && cit.next(pc)) {
+      const int64_t row = s_row[pc.i];
+      // the piece's query slice (requested when the previous piece ended) has landed; its
+      // fragments are read from shared memory per block, which keeps registers for O
+      cp_async_wait_all();
+      __syncwarp();
+      const uint32_t qbase = smem_u32(sQ) + (lane & 15) * C::Q_ROW + (lane >> 4) * 16;
+      const int ctx = s_ctx[pc.i];
+      float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows r0 and r0 + 8 (log2 units)
+      float l_run[2] = {0.f, 0.f};
+      float o[C::VW / 8][4];
+#pragma unroll
+      for (int i = 0; i < C::VW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int j = pc.lo; j < pc.hi; ++j, ++t) {
+        const int s = t % C::NS;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / C::NS) & 1, p.err));
+        uint8_t* sK = smem + s * C::STAGE_BYTES;
+        const uint32_t kbase = smem_u32(sK);
+        // partial S over this warp's 144 dims: 16 heads x 16 tokens as two 8-token n-tiles
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (got) {
+#pragma unroll
+          for (int k = 0; k < C::KSW; ++k) {
+            const int ks = w * C::KSW + k;
+            const int tok = ((lane >> 4) << 3) + (lane & 7);
+            const int chunk = (ks % 4) * 2 + ((lane >> 3) & 1);
+            uint32_t qa[4], b0r, b1r, b2r, b3r;
+            ldsm_x4(qbase + k * 32, qa[0], qa[1], qa[2], qa[3]);
+            ldsm_x4(kbase + (ks / 4) * 2048 + sw128(tok, chunk), b0r, b1r, b2r, b3r);
+            mma_16816(sc[0], qa, b0r, b1r);
+            mma_16816(sc[1], qa, b2r, b3r);
+          }
+        }
+        if (lane == 0) s_gave_up[t & 1][w] = got ? 0 : 1;
+        // the four partial tiles, summed in the same order by every warp; buffer t & 1, laid
+        // out [warp][n-tile][lane][4] so that each quarter-warp stores 128 contiguous bytes
+        {
+          float* xw = xch + ((t & 1) * C::NCW + w) * 256;
+          *reinterpret_cast<float4*>(xw + lane * 4) = make_float4(sc[0][0], sc[0][1], sc[0][2], sc[0][3]);
+          *reinterpret_cast<float4*>(xw + 128 + lane * 4) = make_float4(sc[1][0], sc[1][1], sc[1][2], sc[1][3]);
+        }
+        compute_bar();
+        // every warp takes the same decision from the same four flags (buffer t & 1 is not
+        // rewritten before all four have passed the next barrier)
+        if (s_gave_up[t & 1][0] | s_gave_up[t & 1][1] | s_gave_up[t & 1][2] | s_gave_up[t & 1][3]) {
+          if (lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+        for (int u = 0; u < C::NCW; ++u) {
+          const float* xu = xch + ((t & 1) * C::NCW + u) * 256;
+          const float4 a = *reinterpret_cast<const float4*>(xu + lane * 4);
+          const float4 b = *reinterpret_cast<const float4*>(xu + 128 + lane * 4);
+          sc[0][0] += a.x;
+          sc[0][1] += a.y;
+          sc[0][2] += a.z;
+          sc[0][3] += a.w;
+          sc[1][0] += b.x;
+          sc[1][1] += b.y;
+          sc[1][2] += b.z;
+          sc[1][3] += b.w;
+        }
+        const int valid = min(C::BS, ctx - j * C::BS);  // tokens of this block
+        if (valid < C::BS) {
+          // zero this warp's value rows past the end (its two boxes: the other warps are past
+          // the barrier and read only their own boxes), so that P = 0 meets no non-finite value
+          for (int c2 = lane; c2 < (C::BS - valid) * 16; c2 += 32) {
+            const int rrow = valid + c2 / 16, rest = c2 % 16;
+            *reinterpret_cast<uint4*>(sK + (2 * w + rest / 8) * 2048 + rrow * 128 + (rest % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // online softmax in log2 units (identical state in all four warps)
+        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + 2 * (lane & 3) + (e & 1);
+            if (tok < valid) mx[e >> 1] = fmaxf(mx[e >> 1], sc[nt][e]);
+          }
+        float alpha[2], neg_m[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+          const float m_new = fmaxf(m_run[h], mx[h] * p.scale_log2);
+          alpha[h] = (m_new == -CUDART_INF_F) ? 1.f : ex2_approx(m_run[h] - m_new);
+          m_run[h] = m_new;
+          neg_m[h] = m_new == -CUDART_INF_F ? 0.f : -m_new;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + 2 * (lane & 3) + (e & 1);
+            const float pv = tok < valid ? ex2_approx(fmaf(sc[nt][e], p.scale_log2, neg_m[e >> 1])) : 0.f;
+            sc[nt][e] = pv;
+            rs[e >> 1] += pv;
+          }
+        l_run[0] = l_run[0] * alpha[0] + rs[0];
+        l_run[1] = l_run[1] * alpha[1] + rs[1];
+#pragma unroll
+        for (int i = 0; i < C::VW / 8; ++i) {
+          o[i][0] *= alpha[0];
+          o[i][1] *= alpha[0];
+          o[i][2] *= alpha[1];
+          o[i][3] *= alpha[1];
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+        pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+        pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+        pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+        // O += P V over this warp's 128 value dims (boxes 2w and 2w + 1 of the same rows)
+#pragma unroll
+        for (int nd = 0; nd < C::VW / 16; ++nd) {
+          const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
+          const int d = w * C::VW + nd * 16 + ((lane >> 4) << 3);
+          uint32_t b0r, b1r, b2r, b3r;
+          ldsm_x4_t(kbase + (d / 64) * 2048 + sw128(tok, (d % 64) / 8), b0r, b1r, b2r, b3r);
+          mma_16816(o[2 * nd], pa, b0r, b1r);
+          mma_16816(o[2 * nd + 1], pa, b2r, b3r);
+        }
+        // this warp is done with the stage (reads and any zeroing): release it to the producer
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (pend) flush_arrival();
+      }
+      if (!ok) break;
+      {  // the next piece's query slice, into the buffer this piece has finished reading
+        __syncwarp();
+        PieceIter nx = cit;
+        Piece np;
+        if (nx.next(np)) request_q(s_row[np.i]);
+      }
+      // ---- the piece's result for this warp's slice ----
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+      }
+      const int unit_blocks = (ctx + C::BS - 1) / C::BS;
+      const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
+      const int64_t piece_first = s_pre[pc.i] + pc.lo;
+      const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
+      float inv[2], lse[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+        lse[h] = l_run[h] > 0.f ? (m_run[h] + __log2f(l_run[h])) * 0.69314718055994531f : -CUDART_INF_F;
+      }
+      if (whole) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int gg = r0 + 8 * h;
+          const int hq = hg * C::HG + gg;
+          __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * C::DV + w * C::VW + 2 * (lane & 3);
+#pragma unroll
+          for (int i = 0; i < C::VW / 8; ++i)
+            *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+          if (p.lse && w == 0 && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse[h];
+        }
+        continue;
+      }
+      // a cut piece: merge now if it is the last, else store the partial and arrive later
+      const int c0 = sh.of(s_pre[pc.i]), c1 = sh.of(s_pre[pc.i + 1] - 1), npc = c1 - c0 + 1;
+      unsigned long long* ctr = p.ws_ctr + static_cast<int64_t>(c0) * p.units + unit;
+      unsigned long long cur = 0;
+      if (lane == 0) cur = atomicAdd(ctr, 0ull);
+      if (slot == 1) {
+        const int prior = __shfl_sync(0xffffffffu, static_cast<int>(arrivals_of(cur, p.epoch, npc)), 0);
+        if (prior == npc - 1) {
+          __threadfence();
+          merge_into_registers<C::VW, C::NCW, C::DV>(p, row, unit, c0, c1, c, o, lse, inv, lane);
+          continue;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gg = r0 + 8 * h;
+        float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * p.units + unit) * G + gg) * (C::VW + 4);
+#pragma unroll
+        for (int i = 0; i < C::VW / 8; ++i)
+          *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+        if ((lane & 3) == 0) dst[C::VW] = lse[h];
+      }
+      pend = true;
+      pend_ctr = ctr;
+      pend_cur = cur;
+      pend_np = npc;
+      pend_c0 = c0;
+      pend_c1 = c1;
+      pend_row = row;
+    }
+    if (ok && pend) flush_arrival();
+    if (ok && due > 0) {
+      __threadfence();
+      for (int k = 0; k < due; ++k) merge_pieces<C::VW, C::NCW, C::DV>(p, due_row[k], unit, due_c0[k], due_c1[k], lane);
+    }
+    if (w == 0 && lane == 0) s_used = t;
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  // after a timeout, wait (bounded) for the loads still in flight before the CTA exits
+  if (tid == 0)
+    for (uint32_t i = s_used; i < s_issued; ++i)
+      if (!mbar_wait(&full[i % C::NS], (i / C::NS) & 1, p.err)) break;
+}
+
+// One CTA per share and head group; two CTAs per SM.
+static int mla_shares(int groups) {
+  int sh = num_sms() * 2 / groups;
+  return sh > 0 ? sh : 1;
+}
+
+// Workspace: partials [shares][2 slots][units][16][128 + 4] floats, then the arrival counters
+// [shares][units] (8 bytes each); units = 4 per group of 16 query heads.
+size_t mla_workspace_ctr_offset(int Hq) {
+  const int groups = Hq / MlaCfg::HG;
+  return static_cast<size_t>(mla_shares(groups)) * 2 * groups * MlaCfg::NCW * MlaCfg::HG * (MlaCfg::VW + 4) *
+         sizeof(float);
+}
+size_t mla_workspace_bytes(int Hq) {
+  const int groups = Hq / MlaCfg::HG;
+  return mla_workspace_ctr_offset(Hq) +
+         static_cast<size_t>(mla_shares(groups)) * groups * MlaCfg::NCW * sizeof(unsigned long long);
+}
+
+cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, int* launches) {
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&mla_decode_kernel), MlaCfg::SMEM, kAttrMla);
+  if (e != cudaSuccess) return e;
+  const int groups = p.Hq / MlaCfg::HG;
+  e = launch_pdl(mla_decode_kernel, dim3(mla_shares(groups), groups), dim3(MlaCfg::THREADS), MlaCfg::SMEM, stream,
+                 p, tm);
+  *launches += 1;
+  return e;
+}
+
+}  // namespace pkv

@@ -235,6 +235,51 @@ def write_pack_layers(num_layers: int, T: int, *, Hkv: int, D: int, block_size: 
     return layers
 
 
+@dataclass
+class MlaBatch:
+    """Decode requests over a latent cache: q [B, Hq, Dk]; latent [num_blocks, block_size, 1, Dk]
+    (one latent row per token); block_tables [B, max_blocks]; seq_lens [B]."""
+    q: torch.Tensor
+    latent: torch.Tensor
+    block_tables: torch.Tensor
+    seq_lens: torch.Tensor
+    seq_lens_list: List[int]
+    Hq: int
+    Dk: int
+    block_size: int
+    num_blocks: int
+
+    @property
+    def R(self) -> int:
+        return len(self.seq_lens_list)
+
+
+def mla_batch(B: int, ctx_lo: int, ctx_hi: int, *, Hq: int, Dk: int = 576, block_size: int = 16,
+              pool_factor: float = 1.2, seed: int = 0, device="cpu", q_scale: float = 1.0,
+              seq_lens: Optional[List[int]] = None) -> MlaBatch:
+    """B decode requests against a latent cache (the recipe above, with one latent head of Dk
+    dims per token in place of separate K and V); context lengths uniform in [ctx_lo, ctx_hi]
+    unless given."""
+    g = _cpu_gen(seed)
+    seq = list(seq_lens) if seq_lens is not None else uniform_ints(ctx_lo, ctx_hi, B, g)
+    need = [math.ceil(s / block_size) for s in seq]
+    num_blocks = max(1, math.ceil(pool_factor * sum(need)))
+    max_blocks = max([1] + need)
+    perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    tables = torch.zeros((len(seq), max_blocks), dtype=torch.int32)
+    cur = 0
+    for r, n in enumerate(need):
+        tables[r, :n] = perm[cur:cur + n]
+        cur += n
+    dg = _dev_gen(seed, device)
+    q = randn_bf16((len(seq), Hq, Dk), dg, device, q_scale)
+    latent = randn_bf16((num_blocks, block_size, 1, Dk), dg, device)
+    dev = torch.device(device)
+    return MlaBatch(q=q, latent=latent, block_tables=tables.to(dev),
+                    seq_lens=torch.tensor(seq, dtype=torch.int32, device=dev), seq_lens_list=seq, Hq=Hq,
+                    Dk=Dk, block_size=block_size, num_blocks=num_blocks)
+
+
 def fp8_codes(t: torch.Tensor, scale: float) -> torch.Tensor:
     """E4M3 codes (uint8, same shape and device) standing for t / scale: an FP8 cache's content
     synthesised from values, with torch's float8_e4m3fn conversion (round to nearest even) after
@@ -264,3 +309,10 @@ MIXED_LLAMA70B = dict(n_decode=192, decode_ctx=(1000, 8000), n_extend=8, extend_
 LONG_EXTEND = dict(new_lens=[2048, 2048], ctx_lens=[100000, 100000], Hq=64, Hkv=8, D=128,
                    seed=3)
 WRITE_PACK_LLAMA70B = dict(num_layers=80, T=10000, Hkv=8, D=128, seed=4)
+# DeepSeek-R1-like MLA layer under tensor parallelism 8: 16 query heads per GPU over one
+# 576-wide latent (512 value dims + 64 rotary dims); 128 concurrent requests of a 10K-token
+# prompt part-way through 1K generated tokens. Softmax scale 1/sqrt(128 + 64), the model's
+# query-key head width.
+MLA_DEEPSEEK_TP8 = dict(B=128, ctx_lo=10000, ctx_hi=11000, Hq=16, Dk=576, seed=5)
+MLA_DV = 512
+MLA_SCALE = 1.0 / math.sqrt(192.0)

@@ -101,6 +101,34 @@ def test_decode_workspace_query_is_host_only(lib):
     assert lib.pkv_paged_decode_workspace_size(4, 8, 3, 64, 200) == 0
 
 
+def test_mla_host_checks_without_a_gpu(lib):
+    from paged_kv_attention_reshape_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    reqs = _lib.PkvReqs(None, None, 0, 4, 4)
+    lat = _lib.PkvCache(fake, None, 10, 16, 1, 576, 16 * 576)  # v may be NULL: the rows are shared
+    n = lib.pkv_mla_decode_workspace_size(128, 16, 11000)
+    assert 0 < n <= 64 << 20
+    assert lib.pkv_mla_decode_workspace_size(128, 24, 11000) == 0
+    assert lib.pkv_mla_decode_workspace_size(128, 144, 11000) == 0
+    ws = P(1 << 21)
+    args = lambda c, hq, vd: (fake, c, fake, 4, fake, None, reqs, hq, 100, 0.07, vd, fake, None, ws, n, None)
+    assert lib.pkv_mla_decode_attn(*args(lat, 8, 512)) == 2             # heads not a multiple of 16
+    assert lib.pkv_mla_decode_attn(*args(lat, 16, 256)) == 2            # value width other than 512
+    assert lib.pkv_mla_decode_attn(*args(_lib.PkvCache(fake, None, 10, 16, 2, 576, 16 * 2 * 576), 16, 512)) == 2
+    assert lib.pkv_mla_decode_attn(*args(_lib.PkvCache(fake, None, 10, 16, 1, 512, 16 * 512), 16, 512)) == 2
+    assert lib.pkv_mla_decode_attn(*args(_lib.PkvCache(fake, None, 10, 32, 1, 576, 32 * 576), 16, 512)) == 2
+    fp8 = _lib.PkvCache(fake, None, 10, 16, 1, 576, 16 * 576, _lib.KV_FP8_E4M3, 1.0, 1.0)
+    assert lib.pkv_mla_decode_attn(*args(fp8, 16, 512)) == 2
+    # too small a workspace
+    small = (fake, lat, fake, 4, fake, None, reqs, 16, 100, 0.07, 512, fake, None, ws, n - 16, None)
+    assert lib.pkv_mla_decode_attn(*small) == 3
+    # an empty set is a no-op
+    empty = _lib.PkvReqs(None, None, 0, 0, 4)
+    assert lib.pkv_mla_decode_attn(fake, lat, fake, 4, fake, None, empty, 16, 100, 0.07, 512, fake, None,
+                                   None, 0, None) == 0
+
+
 def test_product_path_has_no_fallback():
     """The binding only calls libpkv.so: it never imports the oracle or torch compute ops."""
     src = open(os.path.join(ROOT, "paged_kv_attention_reshape_gb300", "binding.py")).read()

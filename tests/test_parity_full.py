@@ -79,6 +79,22 @@ def test_decode_qwen3_fp8_full(pkv):
     print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="decode qwen3 fp8 full"))
 
 
+def test_mla_deepseek_tp8_full(pkv):
+    """The MLA decode workload at full size (128 requests over 10K-11K tokens of a 576-wide
+    latent, 16 query heads): 16 sampled requests against the oracle, every head."""
+    b = gen.mla_batch(**gen.MLA_DEEPSEEK_TP8, device="cuda")
+    out, lse = pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, max(b.seq_lens_list),
+                                   gen.MLA_SCALE)
+    torch.cuda.synchronize()
+    assert pkv.device_errors() == 0
+    sample = np.sort(np.random.default_rng(1).choice(b.R, 16, replace=False)).astype(np.int32)
+    ref, ref_lse = oracle.mla_decode(_host(b.q), _host(b.latent), b.block_tables.cpu().numpy(),
+                                     b.seq_lens.cpu().numpy(), gen.MLA_SCALE, gen.MLA_DV, req_ids=sample)
+    rows = np.zeros(b.R, bool)
+    rows[sample] = True
+    print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="mla deepseek tp8 full"))
+
+
 def test_mixed_llama70b_full(pkv):
     """192 decode + 8 extend (512 over 4k-32k) + 4 prefill (2k-8k), shuffled: the full step;
     sampled rows of every class checked."""

@@ -376,6 +376,100 @@ def test_decode_nonfinite_past_the_end_is_ignored(pkv):
     compare_attention(out, lse, ref, ref_lse, what="decode nan tail")
 
 
+# ---- MLA absorbed decode ---------------------------------------------------------------------
+
+def _mla(pkv, b, scale, **kw):
+    return pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, max(b.seq_lens_list), scale, **kw)
+
+
+def _mla_ref(b, scale, latent=None, **kw):
+    lat = bits(b.latent if latent is None else latent)
+    return oracle.mla_decode(bits(b.q), lat, b.block_tables.cpu().numpy(), b.seq_lens.cpu().numpy(), scale,
+                             gen.MLA_DV, **kw)
+
+
+@pytest.mark.parametrize("Hq", [16, 32, 128])
+def test_mla_decode_head_groups(pkv, Hq):
+    """16 query heads per CTA group: one, two and eight groups over the same latent rows."""
+    b = gen.mla_batch(5, 1, 700, Hq=Hq, seed=90 + Hq)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    assert out.shape == (5, Hq, gen.MLA_DV)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what=f"mla Hq={Hq}")
+    assert _errors(pkv) == 0
+
+
+def _to_dev(b):
+    return gen.MlaBatch(**{**b.__dict__, "q": b.q.to(DEV), "latent": b.latent.to(DEV),
+                           "block_tables": b.block_tables.to(DEV), "seq_lens": b.seq_lens.to(DEV)})
+
+
+@pytest.mark.parametrize("ctxs", [[1, 16, 17, 31, 32, 33], [0, 5, 0], [4096, 1, 7000, 15], [30000, 20000]])
+def test_mla_decode_edge_lengths_and_cuts(pkv, ctxs):
+    """Partial last blocks, empty contexts (out 0, lse -inf), and a few long sequences that the
+    shares cut into many pieces (merged in several passes)."""
+    b = gen.mla_batch(len(ctxs), 0, 0, Hq=16, seq_lens=ctxs, seed=len(ctxs) + sum(ctxs) % 97)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what=f"mla {ctxs}")
+    empty = np.array(ctxs) == 0
+    if empty.any():
+        assert np.all(out.float().cpu().numpy()[empty] == 0)
+        assert np.all(np.isneginf(lse.cpu().numpy()[empty]))
+    assert _errors(pkv) == 0
+
+
+def test_mla_decode_peaked_softmax(pkv):
+    b = gen.mla_batch(6, 100, 2000, Hq=16, seed=93, q_scale=3.0)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what="mla peaked")
+
+
+def test_mla_decode_nonfinite_past_the_end_is_ignored(pkv):
+    b = gen.mla_batch(4, 5, 90, Hq=16, seed=94)
+    lat = b.latent.clone()
+    bt = b.block_tables.numpy()
+    for r, n in enumerate(b.seq_lens_list):
+        lat[bt[r, (n - 1) // 16], n % 16 or 16:] = float("nan")
+    out, lse = pkv.mla_decode_attn(b.q.to(DEV), lat.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV),
+                                   max(b.seq_lens_list), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE, latent=lat)
+    compare_attention(out, lse, ref, ref_lse, what="mla nan tail")
+
+
+def test_mla_decode_request_set_and_query_rows(pkv):
+    """A request set given by order/bounds (the decode class of a reordered batch) with query
+    rows taken through cu_q: only the set's rows are written."""
+    R = 9
+    b = gen.mla_batch(R, 1, 900, Hq=16, seed=95)
+    order = torch.tensor([7, 2, 5, 0, 8, 1, 3, 4, 6], dtype=torch.int32)
+    bounds = torch.tensor([2, 7, 9, 9], dtype=torch.int32)  # the set: order[2:7]
+    cu_q = torch.tensor([3 * r for r in range(R + 1)], dtype=torch.int32)  # query row of r = 3r
+    q = gen.randn_bf16((3 * R, 16, 576), torch.Generator().manual_seed(6), "cpu")
+    out = torch.full((3 * R, 16, gen.MLA_DV), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((3 * R, 16), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.mla_decode_attn(q.to(DEV), b.latent.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV),
+                        max(b.seq_lens_list), gen.MLA_SCALE, cu_q=cu_q.to(DEV),
+                        reqs=pkv.Reqs(5, R, order.to(DEV), bounds.to(DEV), 0), out=out, lse=lse)
+    members = order[2:7].numpy()
+    ref, ref_lse = oracle.mla_decode(bits(q), bits(b.latent), b.block_tables.numpy(), b.seq_lens.numpy(),
+                                     gen.MLA_SCALE, gen.MLA_DV, cu_q=cu_q.numpy(), req_ids=members)
+    rows = np.zeros(3 * R, bool)
+    rows[3 * members] = True
+    compare_attention(out, lse, ref, ref_lse, rows=rows, what="mla set")
+    assert torch.isnan(out.float().cpu()[~torch.from_numpy(rows)]).all()
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("Hq,v_dim,dk", [(8, 512, 576), (16, 256, 576), (16, 512, 512), (144, 512, 576)])
+def test_mla_decode_rejects_other_shapes(pkv, Hq, v_dim, dk):
+    b = gen.mla_batch(2, 1, 40, Hq=Hq, Dk=dk, seed=96)
+    with pytest.raises(pkv.PkvError):
+        pkv.mla_decode_attn(b.q.to(DEV), b.latent.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV), 40,
+                            gen.MLA_SCALE, v_dim=v_dim)
+
+
 # ---- extend / prefill ------------------------------------------------------------------------
 
 @pytest.mark.parametrize("G,D", [(1, 64), (4, 128), (8, 128), (16, 64), (2, 128)])

@@ -20,10 +20,12 @@
 //     the previous piece ends, and its MMA fragments are re-read from shared memory for each
 //     block (registers go to the 16 x 128 fp32 output accumulator);
 //   * the 16 heads sit on the M dimension of the warp-level bf16 MMA (m16n8k16, fp32
-//     accumulate). Compute warp w scores dims 144w .. 144w + 143 (its query slice stays in
-//     registers), the four partial 16 x 16 score tiles are summed through shared memory
-//     behind one named barrier (in the same order by every warp, so all four hold identical
-//     scores and softmax state), and warp w accumulates output dims 128w .. 128w + 127;
+//     accumulate). Compute warp w scores the k-steps w, w + 4, .., w + 32 (dims 64i + 16w ..
+//     64i + 16w + 15: the same column pair of each 64-wide box, so every fragment address is
+//     a fixed per-lane offset plus a constant), the four partial 16 x 16 score tiles are
+//     summed through shared memory behind one named barrier (in the same order by every warp,
+//     so all four hold identical scores and softmax state), and warp w accumulates output
+//     dims 128w .. 128w + 127. O is rescaled only when a row's running max grows;
 //   * each warp is one "unit" of the split-KV merge (a 128-wide slice of a 16-head group):
 //     a piece cut at a share edge stores its slice's partial and arrives on its own counter.
 #include <math_constants.h>
@@ -31,6 +33,7 @@
 #include "common.cuh"
 #include "decode_shares.cuh"
 #include "launch.h"
+#include "softmax.cuh"
 
 namespace pkv {
 
@@ -41,7 +44,7 @@ struct MlaCfg {
   static constexpr int HG = 16;                  // query heads per CTA (the MMA's M)
   static constexpr int NCW = 4;                  // compute warps
   static constexpr int THREADS = (NCW + 1) * 32; // + the producer warp
-  static constexpr int KW = DK / NCW;            // 144 scored dims per warp
+  static constexpr int KW = DK / NCW;            // 144 scored dims per warp (9 k-steps)
   static constexpr int KSW = KW / 16;            // 9 k-steps per warp
   static constexpr int VW = DV / NCW;            // 128 output dims per warp
   static constexpr int BOXES = DK / 64;          // 9 TMA boxes per block
@@ -170,19 +173,21 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
     }
     if (lane == 0) s_issued = issued;
   } else {
-    // ============ compute warp w: score dims 144w.., output dims 128w.. of 16 heads ============
+    // ======= compute warp w: k-steps w + 4i of the scores, output dims 128w.. of 16 heads =======
     const int w = warp;
     const int unit = hg * C::NCW + w;  // this warp's unit of the split-KV merge
     const int G = C::HG;
     uint8_t* sQ = smem + C::OFF_Q + w * C::Q_BYTES;
     float* xch = reinterpret_cast<float*>(smem + C::OFF_X);
 
-    // query slice of a row: heads hg*16 .. +15, dims 144w .. 144w + 143, rows padded to 304 B
-    // (ldmatrix rows of a phase then fall on distinct banks)
+    // query slice of a row: heads hg*16 .. +15; chunk pair i of a row holds dims 64i + 16w ..
+    // +15 (k-step w + 4i); rows padded to 304 B (ldmatrix rows of a phase then fall on
+    // distinct banks)
     auto request_q = [&](int64_t row) {
       for (int c16 = lane; c16 < C::HG * (C::KW / 8); c16 += 32) {
         const int gg = c16 / (C::KW / 8), chunk = c16 % (C::KW / 8);
-        const __nv_bfloat16* src = p.q + (row * p.Hq + hg * C::HG + gg) * C::DK + w * C::KW + chunk * 8;
+        const __nv_bfloat16* src =
+            p.q + (row * p.Hq + hg * C::HG + gg) * C::DK + (chunk / 2) * 64 + w * 16 + (chunk % 2) * 8;
         cp_async16(sQ + gg * C::Q_ROW + chunk * 16, src, 16u);
       }
       cp_async_commit();
@@ -224,6 +229,17 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
       }
     };
 
+    // fixed per-lane shared-memory offsets. K fragment of k-step w + 4i: box i, 16-byte chunk
+    // pair w of the box (the same in every box); V fragments of dims 128w + 16nd: box
+    // 2w + nd/4, chunk pair nd % 4.
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t koff = sw128(((lane >> 4) << 3) + (lane & 7), 2 * w + ((lane >> 3) & 1));
+    uint32_t voff[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+      voff[a] = 2 * w * (C::BS * 128) + sw128((((lane >> 3) & 1) << 3) + (lane & 7), 2 * a + (lane >> 4));
+    const int tok0 = 2 * (lane & 3);  // fragment columns tok0, tok0 + 1 (+ 8)
+
     Piece pc;
     uint32_t t = 0;  // blocks consumed
     bool ok = true;
@@ -244,31 +260,38 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
       for (int j = pc.lo; j < pc.hi; ++j, ++t) {
         const int s = t % C::NS;
         const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / C::NS) & 1, p.err));
-        uint8_t* sK = smem + s * C::STAGE_BYTES;
-        const uint32_t kbase = smem_u32(sK);
-        // partial S over this warp's 144 dims: 16 heads x 16 tokens as two 8-token n-tiles
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (got) {
+        const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
+        // partial S over this warp's k-steps w + 4i (dims 64i + 16w .. +15, i = 0..8): 16 heads
+        // x 16 tokens as two 8-token n-tiles, even and odd i in separate accumulators
+        uint64_t sp[2][2][2];  // [chain][n-tile][row half] packed column pairs
+        {
+          float acc[2][2][4] = {};
+          if (got) {
 #pragma unroll
-          for (int k = 0; k < C::KSW; ++k) {
-            const int ks = w * C::KSW + k;
-            const int tok = ((lane >> 4) << 3) + (lane & 7);
-            const int chunk = (ks % 4) * 2 + ((lane >> 3) & 1);
-            uint32_t qa[4], b0r, b1r, b2r, b3r;
-            ldsm_x4(qbase + k * 32, qa[0], qa[1], qa[2], qa[3]);
-            ldsm_x4(kbase + (ks / 4) * 2048 + sw128(tok, chunk), b0r, b1r, b2r, b3r);
-            mma_16816(sc[0], qa, b0r, b1r);
-            mma_16816(sc[1], qa, b2r, b3r);
+            for (int i = 0; i < C::KSW; ++i) {
+              uint32_t qa[4], b0r, b1r, b2r, b3r;
+              ldsm_x4(qbase + i * 32, qa[0], qa[1], qa[2], qa[3]);
+              ldsm_x4(kbase + koff + i * (C::BS * 128), b0r, b1r, b2r, b3r);
+              mma_16816(acc[i & 1][0], qa, b0r, b1r);
+              mma_16816(acc[i & 1][1], qa, b2r, b3r);
+            }
           }
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              sp[c2][nt][0] = sm::f2(acc[c2][nt][0], acc[c2][nt][1]);
+              sp[c2][nt][1] = sm::f2(acc[c2][nt][2], acc[c2][nt][3]);
+            }
+        }
+        // the four warps' partial tiles, summed in the same order by every warp; buffer t & 1,
+        // laid out [warp][n-tile][lane][4] so that each quarter-warp stores 128 contiguous bytes
+        {
+          ulonglong2* xw = reinterpret_cast<ulonglong2*>(xch + ((t & 1) * C::NCW + w) * 256);
+          xw[lane] = make_ulonglong2(sm::add2(sp[0][0][0], sp[1][0][0]), sm::add2(sp[0][0][1], sp[1][0][1]));
+          xw[32 + lane] = make_ulonglong2(sm::add2(sp[0][1][0], sp[1][1][0]), sm::add2(sp[0][1][1], sp[1][1][1]));
         }
         if (lane == 0) s_gave_up[t & 1][w] = got ? 0 : 1;
-        // the four partial tiles, summed in the same order by every warp; buffer t & 1, laid
-        // out [warp][n-tile][lane][4] so that each quarter-warp stores 128 contiguous bytes
-        {
-          float* xw = xch + ((t & 1) * C::NCW + w) * 256;
-          *reinterpret_cast<float4*>(xw + lane * 4) = make_float4(sc[0][0], sc[0][1], sc[0][2], sc[0][3]);
-          *reinterpret_cast<float4*>(xw + 128 + lane * 4) = make_float4(sc[1][0], sc[1][1], sc[1][2], sc[1][3]);
-        }
         compute_bar();
         // every warp takes the same decision from the same four flags (buffer t & 1 is not
         // rewritten before all four have passed the next barrier)
@@ -277,85 +300,103 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
           ok = false;
           break;
         }
+        uint64_t sc[2][2];  // [n-tile][row half]: columns tok0, tok0 + 1 (+ 8 for n-tile 1)
+        {
+          const ulonglong2* xb = reinterpret_cast<const ulonglong2*>(xch + (t & 1) * C::NCW * 256);
+          ulonglong2 a = xb[lane], b = xb[32 + lane];
+          sc[0][0] = a.x;
+          sc[0][1] = a.y;
+          sc[1][0] = b.x;
+          sc[1][1] = b.y;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int u = 1; u < C::NCW; ++u) {
+            a = xb[u * 64 + lane];
+            b = xb[u * 64 + 32 + lane];
+            sc[0][0] = sm::add2(sc[0][0], a.x);
+            sc[0][1] = sm::add2(sc[0][1], a.y);
+            sc[1][0] = sm::add2(sc[1][0], b.x);
+            sc[1][1] = sm::add2(sc[1][1], b.y);
+          }
+        }
+        float f[2][4];  // unpacked scores: f[nt][2h + c], row r0 + 8h, token nt*8 + tok0 + c
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-#pragma unroll
-        for (int u = 0; u < C::NCW; ++u) {
-          const float* xu = xch + ((t & 1) * C::NCW + u) * 256;
-          const float4 a = *reinterpret_cast<const float4*>(xu + lane * 4);
-          const float4 b = *reinterpret_cast<const float4*>(xu + 128 + lane * 4);
-          sc[0][0] += a.x;
-          sc[0][1] += a.y;
-          sc[0][2] += a.z;
-          sc[0][3] += a.w;
-          sc[1][0] += b.x;
-          sc[1][1] += b.y;
-          sc[1][2] += b.z;
-          sc[1][3] += b.w;
+        for (int nt = 0; nt < 2; ++nt) {
+          sm::unf2(sc[nt][0], f[nt][0], f[nt][1]);
+          sm::unf2(sc[nt][1], f[nt][2], f[nt][3]);
         }
         const int valid = min(C::BS, ctx - j * C::BS);  // tokens of this block
         if (valid < C::BS) {
           // zero this warp's value rows past the end (its two boxes: the other warps are past
           // the barrier and read only their own boxes), so that P = 0 meets no non-finite value
+          uint8_t* sK = smem + s * C::STAGE_BYTES;
           for (int c2 = lane; c2 < (C::BS - valid) * 16; c2 += 32) {
             const int rrow = valid + c2 / 16, rest = c2 % 16;
             *reinterpret_cast<uint4*>(sK + (2 * w + rest / 8) * 2048 + rrow * 128 + (rest % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (nt * 8 + tok0 + (e & 1) >= valid) f[nt][e] = -CUDART_INF_F;
         }
-        // online softmax in log2 units (identical state in all four warps)
-        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = nt * 8 + 2 * (lane & 3) + (e & 1);
-            if (tok < valid) mx[e >> 1] = fmaxf(mx[e >> 1], sc[nt][e]);
-          }
-        float alpha[2], neg_m[2];
+        // online softmax in log2 units (identical state in all four warps); O and l are
+        // rescaled only when a row's running max grows (the factor is exactly 1 otherwise)
+        float m_new[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-          const float m_new = fmaxf(m_run[h], mx[h] * p.scale_log2);
-          alpha[h] = (m_new == -CUDART_INF_F) ? 1.f : ex2_approx(m_run[h] - m_new);
-          m_run[h] = m_new;
-          neg_m[h] = m_new == -CUDART_INF_F ? 0.f : -m_new;
+          float mx = sm::max3(f[0][2 * h], f[0][2 * h + 1], fmaxf(f[1][2 * h], f[1][2 * h + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          m_new[h] = fmaxf(m_run[h], mx * p.scale_log2);
         }
-        float rs[2] = {0.f, 0.f};
+        if (__any_sync(0xffffffffu, m_new[0] > m_run[0] || m_new[1] > m_run[1])) {
+          float alpha[2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = nt * 8 + 2 * (lane & 3) + (e & 1);
-            const float pv = tok < valid ? ex2_approx(fmaf(sc[nt][e], p.scale_log2, neg_m[e >> 1])) : 0.f;
-            sc[nt][e] = pv;
-            rs[e >> 1] += pv;
+          for (int h = 0; h < 2; ++h) {
+            alpha[h] = ex2_approx(m_run[h] - m_new[h]);  // 0 on the first block (m_run = -inf)
+            l_run[h] *= alpha[h];
+            m_run[h] = m_new[h];
           }
-        l_run[0] = l_run[0] * alpha[0] + rs[0];
-        l_run[1] = l_run[1] * alpha[1] + rs[1];
 #pragma unroll
-        for (int i = 0; i < C::VW / 8; ++i) {
-          o[i][0] *= alpha[0];
-          o[i][1] *= alpha[0];
-          o[i][2] *= alpha[1];
-          o[i][3] *= alpha[1];
+          for (int i = 0; i < C::VW / 8; ++i) {
+            o[i][0] *= alpha[0];
+            o[i][1] *= alpha[0];
+            o[i][2] *= alpha[1];
+            o[i][3] *= alpha[1];
+          }
         }
         uint32_t pa[4];
-        pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-        pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-        pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-        pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+        {
+          const uint64_t sl = sm::f2(p.scale_log2, p.scale_log2);
+          const uint64_t nm0 = sm::f2(-m_run[0], -m_run[0]), nm1 = sm::f2(-m_run[1], -m_run[1]);
+          uint64_t rsum[2];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            float x[4];
+            sm::unf2(sm::fma2(sm::f2(f[nt][0], f[nt][1]), sl, nm0), x[0], x[1]);
+            sm::unf2(sm::fma2(sm::f2(f[nt][2], f[nt][3]), sl, nm1), x[2], x[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = ex2_approx(x[e]);  // masked: 2^-inf = 0
+            const uint64_t lo = sm::f2(x[0], x[1]), hi = sm::f2(x[2], x[3]);
+            pa[2 * nt] = sm::bf16x2(lo);
+            pa[2 * nt + 1] = sm::bf16x2(hi);
+            rsum[0] = nt == 0 ? lo : sm::add2(rsum[0], lo);
+            rsum[1] = nt == 0 ? hi : sm::add2(rsum[1], hi);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float a, b;
+            sm::unf2(rsum[h], a, b);
+            l_run[h] += a + b;
+          }
+        }
         // O += P V over this warp's 128 value dims (boxes 2w and 2w + 1 of the same rows)
 #pragma unroll
         for (int nd = 0; nd < C::VW / 16; ++nd) {
-          const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
-          const int d = w * C::VW + nd * 16 + ((lane >> 4) << 3);
           uint32_t b0r, b1r, b2r, b3r;
-          ldsm_x4_t(kbase + (d / 64) * 2048 + sw128(tok, (d % 64) / 8), b0r, b1r, b2r, b3r);
+          ldsm_x4_t(kbase + voff[nd % 4] + (nd / 4) * (C::BS * 128), b0r, b1r, b2r, b3r);
           mma_16816(o[2 * nd], pa, b0r, b1r);
           mma_16816(o[2 * nd + 1], pa, b2r, b3r);
         }

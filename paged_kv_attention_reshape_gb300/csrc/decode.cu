@@ -23,13 +23,14 @@
 //     folded in;
 //   * the query tile of the next piece is requested (cp.async) when a piece starts, so it is
 //     in shared memory by the time the warp reaches that piece;
-//   * a piece that covers its whole sequence writes out/lse from registers; a piece cut at a
-//     share edge writes an fp32 partial (normalised O and natural-log LSE, at most two partial
-//     slots per CTA and head) and arrives on a counter of its sequence and KV head; the warp
-//     that arrives last folds the pieces with the LSE merge and writes out/lse. Counters carry
-//     the call's epoch, so a counter left by an earlier call reads as empty and the workspace
-//     needs no clearing. No second kernel, no shared-memory combine, no block-wide barrier
-//     after the prologue.
+//   * a piece that covers its whole sequence writes out/lse from registers; the pieces of a
+//     sequence cut at share edges are merged with the LSE merge along a tree of fan-in 4 (an
+//     fp32 partial per piece: normalised O and natural-log LSE, at most two partial slots per
+//     CTA and head; per tree node an arrival counter, and the arrival that completes a node's
+//     count merges its children), so a long sequence cut into n pieces costs a chain of about
+//     log4(n) small merges. Counters carry the call's epoch, so a counter left by an earlier
+//     call reads as empty and the workspace needs no clearing. No second kernel, no
+//     shared-memory combine, no block-wide barrier after the prologue.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -253,35 +254,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
   for (int s = 0; s < C::NSW; ++s)
     if (more) more = issue_next(s);
 
-  // ---- deferred arrival of the last stored partial ----
-  bool pend = false;
-  unsigned long long* pend_ctr = nullptr;
-  unsigned long long pend_cur = 0;  // lane 0: the counter as read when the piece ended
-  int pend_np = 0, pend_c0 = 0, pend_c1 = 0;
-  int64_t pend_row = 0;
-  // merges this warp owes after its arrivals completed a count (at most one per stored
-  // partial, so at most two per share); run once the share is done
-  int due = 0;
-  int due_c0[2] = {0, 0}, due_c1[2] = {0, 0};
-  int64_t due_row[2] = {0, 0};
-  auto flush_arrival = [&]() {
-    __threadfence();
-    __syncwarp();
-    int arrived = 0;
-    if (lane == 0) arrived = arrive_counter(pend_ctr, p.epoch, pend_np, pend_cur, p.err);
-    arrived = __shfl_sync(0xffffffffu, arrived, 0);
-    pend = false;
-    if (arrived == pend_np) {
-      if (due < 2) {
-        due_c0[due] = pend_c0;
-        due_c1[due] = pend_c1;
-        due_row[due] = pend_row;
-        ++due;
-      } else if (lane == 0) {
-        flag_error(p.err, PKV_DEVERR_REQS);  // cannot happen: a share stores at most two partials
-      }
-    }
-  };
+  // ---- cut sequences: their pieces' partials and the merge tree ----
+  __shared__ CutState s_cut[C::MAXW];
+  CutMerger<D, 1, D> merger(&s_cut[warp], lane);
 
   // ---- compute cursor ----
   Piece pc;
@@ -445,7 +420,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
       fence_proxy_async_smem();
       __syncwarp();
       if (more) more = issue_next(s);
-      if (pend) flush_arrival();
+      if (merger.pend) merger.flush(p, lane);
     }
     if (!ok) break;
     // ---- the piece's result ----
@@ -456,9 +431,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
     }
     const int unit_blocks = (ctx + C::BS - 1) / C::BS;
     const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
-    // partial slot: 0 for a piece that starts this CTA's share inside its sequence, else 1
-    const int64_t piece_first = s_pre[pc.i] + pc.lo;
-    const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
     float inv[2], lse[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -479,46 +451,22 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
       }
       continue;
     }
-    // A cut piece. Its sequence's pieces are those of shares c0 .. c1. A piece that ends this
-    // share first looks whether all the others have arrived: then it is the last and merges
-    // them into its registers, storing nothing of its own. Otherwise it stores its partial
-    // and arrives on the counter after the next block (its stores have completed by then), so
-    // the arrival costs the stream little; the arrival that completes the count merges.
-    const int c0 = sh.of(s_pre[pc.i]), c1 = sh.of(s_pre[pc.i + 1] - 1), npc = c1 - c0 + 1;
-    unsigned long long* ctr = p.ws_ctr + static_cast<int64_t>(c0) * Hkv + kh;
-    unsigned long long cur = 0;
-    if (lane == 0) cur = atomicAdd(ctr, 0ull);
-    if (slot == 1) {
-      const int prior = __shfl_sync(0xffffffffu, static_cast<int>(arrivals_of(cur, p.epoch, npc)), 0);
-      if (prior == npc - 1) {
-        __threadfence();
-        merge_into_registers<D>(p, row, kh, c0, c1, c, o, lse, inv, lane);
-        continue;
-      }
-    }
+    // A cut piece: its normalised partial enters the sequence's merge tree (piece c - c0 of the
+    // shares c0 .. c1 that hold the sequence). A piece that ends the share first looks whether
+    // its siblings are all in (then it merges them in registers); otherwise it stores its
+    // partial and arrives after the next block.
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int gg = r0 + 8 * h;
-      if (gg >= G) continue;
-      float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * Hkv + kh) * G + gg) * (D + 4);
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i)
-        *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
-      if ((lane & 3) == 0) dst[D] = lse[h];
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= inv[0];
+      o[i][1] *= inv[0];
+      o[i][2] *= inv[1];
+      o[i][3] *= inv[1];
     }
-    pend = true;
-    pend_ctr = ctr;
-    pend_cur = cur;
-    pend_np = npc;
-    pend_c0 = c0;
-    pend_c1 = c1;
-    pend_row = row;
+    const int c0 = sh.of(s_pre[pc.i]);
+    const Cut cs{c0, sh.of(s_pre[pc.i + 1] - 1) - c0 + 1, row};
+    merger.piece_done(p, cs, c - c0, kh, o, lse, s_pre[pc.i] + pc.hi == b1, lane);
   }
-  if (ok && pend) flush_arrival();
-  if (ok && due > 0) {
-    __threadfence();
-    for (int k = 0; k < due; ++k) merge_pieces<D>(p, due_row[k], kh, due_c0[k], due_c1[k], lane);
-  }
+  if (ok) merger.finish(p, kh, lane);
   // after a timeout, wait (bounded) for this worker's loads still in flight before exiting
   for (; t < issued; ++t) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[t % C::NSW], (t / C::NSW) & 1, p.err))) break;
@@ -551,13 +499,14 @@ static DecodeShape decode_shape(int Hkv) {
 }
 
 // Workspace: partials [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows
-// padded to 16 bytes), then the arrival counters [shares][Hkv] of cut sequences (8 bytes each).
+// padded to 16 bytes), then the merge-tree counters [levels][shares][2 slots][Hkv] (8 bytes each).
 size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D) {
   return static_cast<size_t>(decode_shape(Hkv).shares) * 2 * Hq * (D + 4) * sizeof(float);
 }
 size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
+  const int shares = decode_shape(Hkv).shares;
   return decode_workspace_ctr_offset(Hq, Hkv, D) +
-         static_cast<size_t>(decode_shape(Hkv).shares) * Hkv * sizeof(unsigned long long);
+         static_cast<size_t>(merge_levels(shares)) * shares * 2 * Hkv * sizeof(unsigned long long);
 }
 
 template <int D, bool FP8>

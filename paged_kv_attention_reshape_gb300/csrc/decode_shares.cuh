@@ -199,146 +199,318 @@ __device__ __forceinline__ int arrive_counter(unsigned long long* ctr, uint32_t 
   return 0;
 }
 
-// The last piece of a cut sequence to finish, with its own result still in registers (the MMA
-// accumulator layout: rows r0 and r0 + 8, columns i*8 + 2*(lane%4) + {0, 1}), folds in the
-// partials of the other pieces (shares c0 .. c1 except `self`) one at a time with the LSE merge
-// (running max, weight sum and sum), and writes out/lse.
-template <int D, int UPG = 1, int OUT_DIM = D>
-__device__ __forceinline__ void merge_into_registers(const DecodeParams& p, int64_t row, int kh, int c0,
-                                                     int c1, int self, float (&o)[D / 8][4],
-                                                     const float (&lse_self)[2], const float (&inv_self)[2],
-                                                     int lane) {
-  const int G = p.G, U = p.units, r0 = lane >> 2, col = 2 * (lane & 3);
+// ---- the merge tree of a cut sequence -----------------------------------------------------------
+// The pieces p = 0 .. np-1 of one unit's cut sequence sit in consecutive shares c0 + p: piece 0
+// is the last piece of share c0 (its partial in slot 1), the others are the first piece of
+// their share (slot 0). They are merged by a tree of fan-in 4: node (L, a) covers pieces
+// [a 4^L, (a + 1) 4^L) and has the children (L - 1, 4a ..); level 0 are the pieces. A node's
+// partial lives where its first piece's partial lives (the merged result overwrites that of
+// its first child), and node (L >= 1, a) counts its children's arrivals on a counter of its
+// own. The child whose arrival completes the count merges them, so a sequence cut into n
+// pieces is merged along a chain of about log4(n) merges of at most four partials each,
+// instead of by one warp reading all n.
+constexpr int kFan = 4;
+
+struct Cut {
+  int c0, np;   // first share, pieces
+  int64_t row;  // query row
+  __device__ int nodes(int L) const { return (np + (1 << (2 * L)) - 1) >> (2 * L); }
+  __device__ int children(int L, int a) const { return min(kFan, nodes(L - 1) - a * kFan); }
+  __device__ int share(int L, int a) const { return c0 + (a << (2 * L)); }
+  __device__ int slot(int a) const { return a == 0 ? 1 : 0; }
+};
+
+// Partial of node (L, a) of unit kh, row gg: [D] normalised O, then the natural-log LSE.
+template <int D>
+__device__ __forceinline__ float* node_part(const DecodeParams& p, const Cut& s, int L, int a, int kh, int gg) {
+  return p.ws_part + (((static_cast<int64_t>(s.share(L, a)) * 2 + s.slot(a)) * p.units + kh) * p.G + gg) * (D + 4);
+}
+// Arrival counter of node (L >= 1, a): [level - 1][share][slot][unit]. A share is the first
+// share of at most one cut sequence (slot 1) and holds the first piece of at most one (slot 0),
+// so no two nodes of a call share a counter.
+__device__ __forceinline__ unsigned long long* node_ctr(const DecodeParams& p, const Cut& s, int L, int a, int kh) {
+  return p.ws_ctr + ((static_cast<int64_t>(L - 1) * gridDim.x + s.share(L, a)) * 2 + s.slot(a)) * p.units + kh;
+}
+// Counter levels a grid of `shares` CTAs needs: 4^levels >= shares.
+__host__ __device__ constexpr int merge_levels(int shares) {
+  int L = 1;
+  while ((1ll << (2 * L)) < shares) ++L;
+  return L;
+}
+
+// A normalised partial in registers, in the MMA accumulator layout: o[i][2h + c] is row
+// r0 + 8h (r0 = lane / 4), column i*8 + 2*(lane%4) + c, and lse[h] the row's LSE.
+// Fold the children of node (L, a) other than `self` (its index among them) into the
+// registers, which hold child `self`; the registers then hold node (L, a).
+template <int D>
+__device__ __forceinline__ void fold_siblings(const DecodeParams& p, const Cut& s, int L, int a, int k, int self,
+                                              int kh, float (&o)[D / 8][4], float (&lse)[2], int lane) {
+  const int G = p.G, r0 = lane >> 2, col = 2 * (lane & 3);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int gg = r0 + 8 * h;
     if (gg >= G) continue;
-    float M = lse_self[h], W = lse_self[h] == -CUDART_INF_F ? 0.f : 1.f;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][2 * h] *= inv_self[h];
-      o[i][2 * h + 1] *= inv_self[h];
-    }
-    for (int cc = c0; cc <= c1; ++cc) {
-      if (cc == self) continue;
-      const float* src = p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * U + kh) * G + gg) * (D + 4);
+    float M = lse[h], W = lse[h] == -CUDART_INF_F ? 0.f : 1.f;
+    for (int m = 0; m < k; ++m) {
+      if (m == self) continue;
+      const float* src = node_part<D>(p, s, L - 1, a * kFan + m, kh, gg);
       const float l = __ldcg(src + D);
       float2 v[D / 8];
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) v[i] = __ldcg(reinterpret_cast<const float2*>(src + i * 8 + col));
       if (l == -CUDART_INF_F) continue;
       const float m_new = fmaxf(M, l);
-      const float a = __expf(M - m_new), w = __expf(l - m_new);
-      W = W * a + w;
+      const float al = __expf(M - m_new), w = __expf(l - m_new);
+      W = W * al + w;
       M = m_new;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) {
-        o[i][2 * h] = o[i][2 * h] * a + w * v[i].x;
-        o[i][2 * h + 1] = o[i][2 * h + 1] * a + w * v[i].y;
+        o[i][2 * h] = o[i][2 * h] * al + w * v[i].x;
+        o[i][2 * h + 1] = o[i][2 * h + 1] * al + w * v[i].y;
       }
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
-    const int hq = out_head<UPG>(p, kh, gg);
-    __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, row, kh, gg) + col;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-      *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
-    if (p.lse && (lane & 3) == 0 && kh % UPG == 0)
-      p.lse[row * p.Hq + hq] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][2 * h] *= inv;
+      o[i][2 * h + 1] *= inv;
+    }
+    lse[h] = W > 0.f ? M + __logf(W) : -CUDART_INF_F;
   }
 }
 
-// LSE merge of the partials of one cut sequence, KV head kh, all of them in the workspace (the
-// path of a piece whose arrival, made after it stored its partial, turned out to be the last):
-// the pieces of shares c0 .. c1 (share c0 holds the sequence's first piece in its slot 1; the
-// later shares hold theirs in slot 0, the first piece of their share). One warp. Lane g < G turns query head g's LSEs into
-// weights; then, four heads at a time, every lane loads its elements l*PER .. l*PER+PER-1 of
-// all their pieces before folding them, so each group costs one round trip to L2 (the partials
-// were written by other SMs and are read from L2). A sequence cut into more than MAXP pieces
-// takes several passes, each adding to the fp32 sum the previous one left in the first piece's
-// partial.
-template <int D, int UPG = 1, int OUT_DIM = D>
-__device__ __forceinline__ void merge_pieces(const DecodeParams& p, int64_t row, int kh, int c0, int c1,
-                                             int lane) {
-  constexpr int PER = D / 32;
-  constexpr int MAXP = 4;  // pieces per pass
-  constexpr int HB = 4;    // heads per group of loads
-  const int G = p.G, U = p.units;
-  const int np = c1 - c0 + 1;
-  auto part = [&](int cc, int gg) {
-    return p.ws_part + (((static_cast<int64_t>(cc) * 2 + (cc == c0 ? 1 : 0)) * U + kh) * G + gg) * (D + 4);
-  };
-  // lane g: max and sum of weights over all pieces of head g
-  float M = -CUDART_INF_F, W = 0.f;
-  if (lane < G) {
-#pragma unroll 4
-    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldcg(part(cc, lane) + D));
-#pragma unroll 4
-    for (int cc = c0; cc <= c1; ++cc) {
-      const float l = __ldcg(part(cc, lane) + D);
-      W += (l == -CUDART_INF_F) ? 0.f : __expf(l - M);
-    }
+// out/lse of the cut sequence from registers (the merge's root).
+template <int D, int UPG, int OUT_DIM>
+__device__ __forceinline__ void write_out_regs(const DecodeParams& p, const Cut& s, int kh, float (&o)[D / 8][4], float (&lse)[2],
+                                               int lane) {
+  const int r0 = lane >> 2, col = 2 * (lane & 3);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int gg = r0 + 8 * h;
+    if (gg >= p.G) continue;
+    __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg) + col;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h], o[i][2 * h + 1]);
+    if (p.lse && (lane & 3) == 0 && kh % UPG == 0) p.lse[s.row * p.Hq + out_head<UPG>(p, kh, gg)] = lse[h];
   }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  for (int pb = 0; pb < np; pb += MAXP) {
-    float w[MAXP];
+}
+
+// The registers as the partial of node (L, a).
+template <int D>
+__device__ __forceinline__ void store_regs(const DecodeParams& p, const Cut& s, int L, int a, int kh,
+                                           float (&o)[D / 8][4], float (&lse)[2], int lane) {
+  const int r0 = lane >> 2, col = 2 * (lane & 3);
 #pragma unroll
-    for (int k = 0; k < MAXP; ++k) {
-      w[k] = 0.f;
-      if (lane < G && pb + k < np) {
-        const float l = __ldcg(part(c0 + pb + k, lane) + D);
-        w[k] = (l == -CUDART_INF_F) ? 0.f : __expf(l - M) * inv;
+  for (int h = 0; h < 2; ++h) {
+    const int gg = r0 + 8 * h;
+    if (gg >= p.G) continue;
+    float* dst = node_part<D>(p, s, L, a, kh, gg);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<float2*>(dst + i * 8 + col) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
+    if ((lane & 3) == 0) dst[D] = lse[h];
+  }
+}
+
+// Merge the k <= 4 children of node (L, a), all in the workspace, into out/lse (the root) or
+// into the node's partial. One warp: lane g < G turns head g's LSEs into weights; then, four
+// heads at a time, every lane loads its elements l*PER .. l*PER+PER-1 of all children before
+// folding them, so each group costs one round trip to L2 (the partials were written by other
+// SMs and are read from L2).
+template <int D, int UPG, int OUT_DIM>
+__device__ __forceinline__ void merge_node(const DecodeParams& p, const Cut& s, int L, int a, int k, bool root,
+                                           int kh, int lane) {
+  constexpr int PER = D / 32;
+  constexpr int HB = 4;  // heads per group of loads
+  const int G = p.G;
+  float M = -CUDART_INF_F, W = 0.f, w[kFan];
+  if (lane < G) {
+    float l[kFan];
+#pragma unroll
+    for (int m = 0; m < kFan; ++m) {
+      l[m] = m < k ? __ldcg(node_part<D>(p, s, L - 1, a * kFan + m, kh, lane) + D) : -CUDART_INF_F;
+      M = fmaxf(M, l[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < kFan; ++m) {
+      w[m] = l[m] == -CUDART_INF_F ? 0.f : __expf(l[m] - M);
+      W += w[m];
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+    for (int m = 0; m < kFan; ++m) w[m] *= inv;
+  } else {
+#pragma unroll
+    for (int m = 0; m < kFan; ++m) w[m] = 0.f;
+  }
+  for (int g0 = 0; g0 < G; g0 += HB) {
+    float v[HB][kFan][PER];
+#pragma unroll
+    for (int hb = 0; hb < HB; ++hb) {
+      const int gg = g0 + hb;
+#pragma unroll
+      for (int m = 0; m < kFan; ++m) {
+        const bool use = gg < G && m < k;
+        const float* src = node_part<D>(p, s, L - 1, a * kFan + (use ? m : 0), kh, use ? gg : 0) + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) {
+          float2 x = make_float2(0.f, 0.f);
+          if (use) x = __ldcg(reinterpret_cast<const float2*>(src + e));
+          v[hb][m][e] = x.x;
+          v[hb][m][e + 1] = x.y;
+        }
       }
     }
-    const bool last_pass = pb + MAXP >= np;
-    for (int g0 = 0; g0 < G; g0 += HB) {
-      float v[HB][MAXP + 1][PER];
 #pragma unroll
-      for (int hb = 0; hb < HB; ++hb) {
-        const int gg = g0 + hb;
+    for (int hb = 0; hb < HB; ++hb) {
+      const int gg = g0 + hb;
+      float acc[PER];
 #pragma unroll
-        for (int k = 0; k <= MAXP; ++k) {
-          // k < MAXP: piece pb + k; k == MAXP: the previous pass's sum
-          const bool use = gg < G && (k < MAXP ? pb + k < np : pb > 0);
-          const float* src = (k < MAXP ? part(c0 + pb + k, gg) : part(c0, gg)) + lane * PER;
+      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll
-          for (int e = 0; e < PER; e += 2) {
-            float2 x = make_float2(0.f, 0.f);
-            if (use) x = __ldcg(reinterpret_cast<const float2*>(src + e));
-            v[hb][k][e] = x.x;
-            v[hb][k][e + 1] = x.y;
-          }
-        }
+      for (int m = 0; m < kFan; ++m) {
+        const float wm = __shfl_sync(0xffffffffu, w[m], gg & 31);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += wm * v[hb][m][e];
       }
+      const float Mg = __shfl_sync(0xffffffffu, M, gg & 31), Wg = __shfl_sync(0xffffffffu, W, gg & 31);
+      if (gg >= G) continue;
+      const float lse = Wg > 0.f ? Mg + __logf(Wg) : -CUDART_INF_F;
+      if (root) {
+        __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg) + lane * PER;
 #pragma unroll
-      for (int hb = 0; hb < HB; ++hb) {
-        const int gg = g0 + hb;
-        float acc[PER];
+        for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e], acc[e + 1]);
+        if (p.lse && lane == 0 && kh % UPG == 0) p.lse[s.row * p.Hq + out_head<UPG>(p, kh, gg)] = lse;
+      } else {
+        float* dst = node_part<D>(p, s, L, a, kh, gg);
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = v[hb][MAXP][e];
-#pragma unroll
-        for (int k = 0; k < MAXP; ++k) {
-          const float wk = __shfl_sync(0xffffffffu, w[k], gg & 31);
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] += wk * v[hb][k][e];
-        }
-        const float Mg = __shfl_sync(0xffffffffu, M, gg & 31), Wg = __shfl_sync(0xffffffffu, W, gg & 31);
-        if (gg >= G) continue;
-        if (!last_pass) {
-          float* keep = part(c0, gg) + lane * PER;
-#pragma unroll
-          for (int e = 0; e < PER; ++e) __stcg(keep + e, acc[e]);
-        } else {
-          const int hq = out_head<UPG>(p, kh, gg);
-          __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, row, kh, gg) + lane * PER;
-#pragma unroll
-          for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e], acc[e + 1]);
-          if (p.lse && lane == 0 && kh % UPG == 0)
-            p.lse[row * p.Hq + hq] = Wg > 0.f ? Mg + __logf(Wg) : -CUDART_INF_F;
-        }
+        for (int e = 0; e < PER; ++e) __stcg(dst + lane * PER + e, acc[e]);
+        if (lane == 0) __stcg(dst + D, lse);
       }
     }
   }
 }
+
+// Merge bookkeeping of one warp, kept in shared memory (it is touched once per piece, and
+// registers are what the streaming loop needs): the owed arrival and the owed merges.
+struct CutState {
+  unsigned long long* pend_ctr;
+  unsigned long long pend_cur;  // the counter as lane 0 read it before the partial was stored
+  Cut pend_s;
+  int pend_L, pend_a, pend_k;
+  int due;                      // nodes whose count this warp completed: merge them at the end
+  Cut due_s[2];
+  int due_L[2], due_a[2];
+};
+
+// The merge work of one warp for one unit kh: finished cut pieces enter the tree, arrivals are
+// deferred by one block (so that the stores before them have drained), and the merges they
+// complete run when the warp's share is done.
+template <int D, int UPG, int OUT_DIM>
+struct CutMerger {
+  CutState* st;       // this warp's state (shared memory)
+  bool pend = false;  // an arrival is owed
+
+  __device__ explicit CutMerger(CutState* state, int lane) : st(state) {
+    if (lane == 0) st->due = 0;
+    __syncwarp();
+  }
+
+  // A cut piece is done: its normalised partial is in (o, lse). Climb while all siblings are
+  // in (folding them into the registers); at the root write out/lse, else store the registers
+  // as the node's partial and owe an arrival on the parent. `check` = look at the counters
+  // first (worth a round trip only when no block of the share follows to hide it).
+  __device__ void piece_done(const DecodeParams& p, const Cut& s, int piece, int kh, float (&o)[D / 8][4],
+                             float (&lse)[2], bool check, int lane) {
+    int L = 1, ai = piece;  // the registers hold node (L - 1, ai)
+    for (;;) {
+      const int a = ai / kFan, k = s.children(L, a);
+      if (k > 1) {
+        unsigned long long* ctr = node_ctr(p, s, L, a, kh);
+        unsigned long long cur = 0;
+        if (lane == 0) cur = atomicAdd(ctr, 0ull);
+        const int prior = check ? __shfl_sync(0xffffffffu, static_cast<int>(arrivals_of(cur, p.epoch, k)), 0) : 0;
+        if (prior != k - 1) {
+          store_regs<D>(p, s, L - 1, ai, kh, o, lse, lane);
+          if (lane == 0) {
+            st->pend_ctr = ctr;
+            st->pend_cur = cur;
+            st->pend_s = s;
+            st->pend_L = L;
+            st->pend_a = a;
+            st->pend_k = k;
+          }
+          __syncwarp();
+          pend = true;
+          return;
+        }
+        __threadfence();
+        fold_siblings<D>(p, s, L, a, k, ai - a * kFan, kh, o, lse, lane);
+        check = true;  // the siblings were in: the next level is likely complete too
+      }
+      if (s.nodes(L) == 1) {
+        write_out_regs<D, UPG, OUT_DIM>(p, s, kh, o, lse, lane);
+        return;
+      }
+      ai = a;
+      ++L;
+    }
+  }
+
+  // The owed arrival (after a block, or at the end): the arrival that completes a count makes
+  // this warp the node's merger.
+  __device__ void flush(const DecodeParams& p, int lane) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      const int k = st->pend_k;
+      if (arrive_counter(st->pend_ctr, p.epoch, k, st->pend_cur, p.err) == k) {
+        const int d = st->due;
+        if (d < 2) {
+          st->due_s[d] = st->pend_s;
+          st->due_L[d] = st->pend_L;
+          st->due_a[d] = st->pend_a;
+          st->due = d + 1;
+        } else {
+          flag_error(p.err, PKV_DEVERR_REQS);  // cannot happen: a share stores at most two partials
+        }
+      }
+    }
+    __syncwarp();
+    pend = false;
+  }
+
+  // The owed merges, each followed up the tree for as long as this warp's arrival completes
+  // the parent's count.
+  __device__ void finish(const DecodeParams& p, int kh, int lane) {
+    if (pend) flush(p, lane);
+    const int due = st->due;
+    if (due == 0) return;
+    __threadfence();
+    for (int d = 0; d < due; ++d) {
+      const Cut s = st->due_s[d];
+      int L = st->due_L[d], a = st->due_a[d];
+      for (;;) {
+        const bool root = s.nodes(L) == 1;
+        merge_node<D, UPG, OUT_DIM>(p, s, L, a, s.children(L, a), root, kh, lane);
+        if (root) break;
+        // the parent with more than one child (a lone child is its parent)
+        int k;
+        do {
+          a /= kFan;
+          ++L;
+          k = s.children(L, a);
+        } while (k == 1);
+        __threadfence();
+        __syncwarp();
+        int arrived = 0;
+        if (lane == 0) arrived = arrive_counter(node_ctr(p, s, L, a, kh), p.epoch, k, 0ull, p.err);
+        if (__shfl_sync(0xffffffffu, arrived, 0) != k) break;
+        __threadfence();
+      }
+    }
+  }
+};
 
 }  // namespace pkv

@@ -27,7 +27,8 @@
 //     so all four hold identical scores and softmax state), and warp w accumulates output
 //     dims 128w .. 128w + 127. O is rescaled only when a row's running max grows;
 //   * each warp is one "unit" of the split-KV merge (a 128-wide slice of a 16-head group):
-//     a piece cut at a share edge stores its slice's partial and arrives on its own counter.
+//     the pieces of a sequence cut at share edges enter the same fan-in-4 merge tree as in
+//     the decode kernel, slice by slice.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
   __shared__ int s_gave_up[2][C::NCW];  // per block (two buffers): compute warp w gave up waiting
   __shared__ int s_abort;               // the compute warps stopped: the producer stops too
   __shared__ uint32_t s_issued, s_used;
+  __shared__ CutState s_cut[C::NCW];
 
   pdl_wait();
   pdl_release();
@@ -201,33 +203,8 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
       if (nx.next(first)) request_q(s_row[first.i]);
     }
 
-    // ---- deferred arrival of the last stored partial (as in the decode kernel) ----
-    bool pend = false;
-    unsigned long long* pend_ctr = nullptr;
-    unsigned long long pend_cur = 0;
-    int pend_np = 0, pend_c0 = 0, pend_c1 = 0;
-    int64_t pend_row = 0;
-    int due = 0;
-    int due_c0[2] = {0, 0}, due_c1[2] = {0, 0};
-    int64_t due_row[2] = {0, 0};
-    auto flush_arrival = [&]() {
-      __threadfence();
-      __syncwarp();
-      int arrived = 0;
-      if (lane == 0) arrived = arrive_counter(pend_ctr, p.epoch, pend_np, pend_cur, p.err);
-      arrived = __shfl_sync(0xffffffffu, arrived, 0);
-      pend = false;
-      if (arrived == pend_np) {
-        if (due < 2) {
-          due_c0[due] = pend_c0;
-          due_c1[due] = pend_c1;
-          due_row[due] = pend_row;
-          ++due;
-        } else if (lane == 0) {
-          flag_error(p.err, PKV_DEVERR_REQS);  // cannot happen: a share stores at most two partials
-        }
-      }
-    };
+    // ---- cut sequences: their pieces' partials and the merge tree ----
+    CutMerger<C::VW, C::NCW, C::DV> merger(&s_cut[w], lane);
 
     // fixed per-lane shared-memory offsets. K fragment of k-step w + 4i: box i, 16-byte chunk
     // pair w of the box (the same in every box); V fragments of dims 128w + 16nd: box
@@ -404,7 +381,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (pend) flush_arrival();
+        if (merger.pend) merger.flush(p, lane);
       }
       if (!ok) break;
       {  // the next piece's query slice, into the buffer this piece has finished reading
@@ -421,8 +398,6 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
       }
       const int unit_blocks = (ctx + C::BS - 1) / C::BS;
       const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
-      const int64_t piece_first = s_pre[pc.i] + pc.lo;
-      const int slot = (piece_first == b0 && pc.lo != 0) ? 0 : 1;
       float inv[2], lse[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -442,41 +417,19 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
         }
         continue;
       }
-      // a cut piece: merge now if it is the last, else store the partial and arrive later
-      const int c0 = sh.of(s_pre[pc.i]), c1 = sh.of(s_pre[pc.i + 1] - 1), npc = c1 - c0 + 1;
-      unsigned long long* ctr = p.ws_ctr + static_cast<int64_t>(c0) * p.units + unit;
-      unsigned long long cur = 0;
-      if (lane == 0) cur = atomicAdd(ctr, 0ull);
-      if (slot == 1) {
-        const int prior = __shfl_sync(0xffffffffu, static_cast<int>(arrivals_of(cur, p.epoch, npc)), 0);
-        if (prior == npc - 1) {
-          __threadfence();
-          merge_into_registers<C::VW, C::NCW, C::DV>(p, row, unit, c0, c1, c, o, lse, inv, lane);
-          continue;
-        }
-      }
+      // a cut piece: its normalised partial enters the sequence's merge tree (this warp's unit)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int gg = r0 + 8 * h;
-        float* dst = p.ws_part + (((static_cast<int64_t>(c) * 2 + slot) * p.units + unit) * G + gg) * (C::VW + 4);
-#pragma unroll
-        for (int i = 0; i < C::VW / 8; ++i)
-          *reinterpret_cast<float2*>(dst + i * 8 + 2 * (lane & 3)) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
-        if ((lane & 3) == 0) dst[C::VW] = lse[h];
+      for (int i = 0; i < C::VW / 8; ++i) {
+        o[i][0] *= inv[0];
+        o[i][1] *= inv[0];
+        o[i][2] *= inv[1];
+        o[i][3] *= inv[1];
       }
-      pend = true;
-      pend_ctr = ctr;
-      pend_cur = cur;
-      pend_np = npc;
-      pend_c0 = c0;
-      pend_c1 = c1;
-      pend_row = row;
+      const int c0 = sh.of(s_pre[pc.i]);
+      const Cut cs{c0, sh.of(s_pre[pc.i + 1] - 1) - c0 + 1, row};
+      merger.piece_done(p, cs, c - c0, unit, o, lse, s_pre[pc.i] + pc.hi == b1, lane);
     }
-    if (ok && pend) flush_arrival();
-    if (ok && due > 0) {
-      __threadfence();
-      for (int k = 0; k < due; ++k) merge_pieces<C::VW, C::NCW, C::DV>(p, due_row[k], unit, due_c0[k], due_c1[k], lane);
-    }
+    if (ok) merger.finish(p, unit, lane);
     if (w == 0 && lane == 0) s_used = t;
     cp_async_wait_all();
   }
@@ -493,8 +446,8 @@ static int mla_shares(int groups) {
   return sh > 0 ? sh : 1;
 }
 
-// Workspace: partials [shares][2 slots][units][16][128 + 4] floats, then the arrival counters
-// [shares][units] (8 bytes each); units = 4 per group of 16 query heads.
+// Workspace: partials [shares][2 slots][units][16][128 + 4] floats, then the merge-tree
+// counters [levels][shares][2 slots][units] (8 bytes each); units = 4 per group of 16 heads.
 size_t mla_workspace_ctr_offset(int Hq) {
   const int groups = Hq / MlaCfg::HG;
   return static_cast<size_t>(mla_shares(groups)) * 2 * groups * MlaCfg::NCW * MlaCfg::HG * (MlaCfg::VW + 4) *
@@ -502,8 +455,9 @@ size_t mla_workspace_ctr_offset(int Hq) {
 }
 size_t mla_workspace_bytes(int Hq) {
   const int groups = Hq / MlaCfg::HG;
+  const int shares = mla_shares(groups);
   return mla_workspace_ctr_offset(Hq) +
-         static_cast<size_t>(mla_shares(groups)) * groups * MlaCfg::NCW * sizeof(unsigned long long);
+         static_cast<size_t>(merge_levels(shares)) * shares * 2 * groups * MlaCfg::NCW * sizeof(unsigned long long);
 }
 
 cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, int* launches) {

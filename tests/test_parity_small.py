@@ -348,6 +348,21 @@ def test_decode_edge_lengths_and_splits(pkv, ctxs):
         assert np.all(o == 0) and np.all(np.isneginf(lse.cpu().numpy()[empty]))
 
 
+@pytest.mark.parametrize("ctxs", [[256], [640], [2048], [2176], [8320], [80000], [192000], [50000, 7, 30000]])
+def test_decode_long_sequences_merge_tree(pkv, ctxs):
+    """A few long sequences spread over all the CTAs: each is cut into up to one piece per
+    share, and the pieces are merged along the fan-in-4 tree (depths 1 to 6 here, including
+    partly filled groups)."""
+    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=1, D=128, seed=sum(ctxs) % 101)
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, max(ctxs),
+                                     cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode long {ctxs}")
+    assert _errors(pkv) == 0
+
+
 def test_decode_peaked_softmax(pkv):
     b = gen.decode_batch(8, 100, 900, Hq=32, Hkv=4, D=128, seed=77, q_scale=4.0)
     g = b.to(DEV)
@@ -416,6 +431,15 @@ def test_mla_decode_edge_lengths_and_cuts(pkv, ctxs):
     if empty.any():
         assert np.all(out.float().cpu().numpy()[empty] == 0)
         assert np.all(np.isneginf(lse.cpu().numpy()[empty]))
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("ctxs", [[640], [8320], [80000], [3, 41000, 9000]])
+def test_mla_decode_long_sequences_merge_tree(pkv, ctxs):
+    b = gen.mla_batch(len(ctxs), 0, 0, Hq=16, seq_lens=ctxs, seed=sum(ctxs) % 89)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what=f"mla long {ctxs}")
     assert _errors(pkv) == 0
 
 

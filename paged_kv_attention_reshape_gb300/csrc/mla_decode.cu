@@ -279,20 +279,29 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
         }
         uint64_t sc[2][2];  // [n-tile][row half]: columns tok0, tok0 + 1 (+ 8 for n-tile 1)
         {
+          // this warp's own partial comes from registers (same values, same order of sums)
           const ulonglong2* xb = reinterpret_cast<const ulonglong2*>(xch + (t & 1) * C::NCW * 256);
-          ulonglong2 a = xb[lane], b = xb[32 + lane];
-          sc[0][0] = a.x;
-          sc[0][1] = a.y;
-          sc[1][0] = b.x;
-          sc[1][1] = b.y;
+          const uint64_t own[2][2] = {{sm::add2(sp[0][0][0], sp[1][0][0]), sm::add2(sp[0][0][1], sp[1][0][1])},
+                                      {sm::add2(sp[0][1][0], sp[1][1][0]), sm::add2(sp[0][1][1], sp[1][1][1])}};
 #pragma unroll
-          for (int u = 1; u < C::NCW; ++u) {
-            a = xb[u * 64 + lane];
-            b = xb[u * 64 + 32 + lane];
-            sc[0][0] = sm::add2(sc[0][0], a.x);
-            sc[0][1] = sm::add2(sc[0][1], a.y);
-            sc[1][0] = sm::add2(sc[1][0], b.x);
-            sc[1][1] = sm::add2(sc[1][1], b.y);
+          for (int u = 0; u < C::NCW; ++u) {
+            uint64_t x[2][2];
+            if (u == w) {
+              x[0][0] = own[0][0];
+              x[0][1] = own[0][1];
+              x[1][0] = own[1][0];
+              x[1][1] = own[1][1];
+            } else {
+              const ulonglong2 a = xb[u * 64 + lane], b = xb[u * 64 + 32 + lane];
+              x[0][0] = a.x;
+              x[0][1] = a.y;
+              x[1][0] = b.x;
+              x[1][1] = b.y;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) sc[nt][hh] = u == 0 ? x[nt][hh] : sm::add2(sc[nt][hh], x[nt][hh]);
           }
         }
         float f[2][4];  // unpacked scores: f[nt][2h + c], row r0 + 8h, token nt*8 + tok0 + c

@@ -22,10 +22,11 @@
 //   * the 16 heads sit on the M dimension of the warp-level bf16 MMA (m16n8k16, fp32
 //     accumulate). Compute warp w scores the k-steps w, w + 4, .., w + 32 (dims 64i + 16w ..
 //     64i + 16w + 15: the same column pair of each 64-wide box, so every fragment address is
-//     a fixed per-lane offset plus a constant), the four partial 16 x 16 score tiles are
-//     summed through shared memory behind one named barrier (in the same order by every warp,
-//     so all four hold identical scores and softmax state), and warp w accumulates output
-//     dims 128w .. 128w + 127. O is rescaled only when a row's running max grows;
+//     a fixed per-lane offset plus a constant) and stores its partial 16 x 16 score tile;
+//     behind a named barrier, warp w sums the four partials of heads 4w .. 4w + 3 (in a fixed
+//     order) and runs their online softmax, writing P (bf16) and the heads' rescale factors;
+//     behind a second barrier every warp takes P as its A fragment and accumulates output
+//     dims 128w .. 128w + 127. O is rescaled only when a head's running max grows;
 //   * each warp is one "unit" of the split-KV merge (a 128-wide slice of a 16-head group):
 //     the pieces of a sequence cut at share edges enter the same fan-in-4 merge tree as in
 //     the decode kernel, slice by slice.
@@ -53,7 +54,7 @@ struct MlaCfg {
   static constexpr int NS = 3;                   // ring stages (two CTAs fit on an SM)
   static constexpr int Q_ROW = KW * 2 + 16;      // 304: a query slice row, padded off the banks
   static constexpr int Q_BYTES = HG * Q_ROW;     // per compute warp
-  static constexpr int XCHG_BYTES = 2 * NCW * 32 * 8 * 4;  // two buffers of partial scores
+  static constexpr int XCHG_BYTES = NCW * 16 * 24 * 4 + 16 * 48;  // partial scores, then P
   static constexpr int MAXR = 1024;              // requests per set handled on device
   static constexpr int MIN_BLOCKS = 8;           // smallest share a CTA is given
   static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;
@@ -83,7 +84,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NS;
   __shared__ int s_scan[C::NCW + 1];
-  __shared__ int s_gave_up[2][C::NCW];  // per block (two buffers): compute warp w gave up waiting
+  __shared__ int s_gave_up[C::NCW];  // per block: compute warp w gave up waiting
+  __shared__ int s_grow[C::NCW];     // per block: a running max of warp w's rows grew
+  __shared__ float s_alpha[C::HG];   // per block: the rescale factor of each head's O
+  __shared__ float s_lm[C::HG][2];   // per piece: each head's running max (log2) and sum
   __shared__ int s_abort;               // the compute warps stopped: the producer stops too
   __shared__ uint32_t s_issued, s_used;
   __shared__ CutState s_cut[C::NCW];
@@ -178,9 +182,10 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
     // ======= compute warp w: k-steps w + 4i of the scores, output dims 128w.. of 16 heads =======
     const int w = warp;
     const int unit = hg * C::NCW + w;  // this warp's unit of the split-KV merge
-    const int G = C::HG;
     uint8_t* sQ = smem + C::OFF_Q + w * C::Q_BYTES;
-    float* xch = reinterpret_cast<float*>(smem + C::OFF_X);
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_X);  // partial scores [warp][16 rows][24]
+    uint8_t* sP = smem + C::OFF_X + C::NCW * 16 * 24 * 4;      // P: 16 rows of 48 bytes (bf16 x 16 + pad)
+    const int srow = 4 * w + (lane >> 3), stok = 2 * (lane & 7);  // this lane's softmax row and tokens
 
     // query slice of a row: heads hg*16 .. +15; chunk pair i of a row holds dims 64i + 16w ..
     // +15 (k-step w + 4i); rows padded to 304 B (ldmatrix rows of a phase then fall on
@@ -229,18 +234,19 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
       __syncwarp();
       const uint32_t qbase = smem_u32(sQ) + (lane & 15) * C::Q_ROW + (lane >> 4) * 16;
       const int ctx = s_ctx[pc.i];
-      float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows r0 and r0 + 8 (log2 units)
-      float l_run[2] = {0.f, 0.f};
       float o[C::VW / 8][4];
 #pragma unroll
       for (int i = 0; i < C::VW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      // softmax state of this lane's row R = 4w + lane/8 (tokens T, T + 1 of each block); the
+      // four lanes' partial sums of l are added at the piece end
+      float m_row = -CUDART_INF_F, l_lane = 0.f;
       for (int j = pc.lo; j < pc.hi; ++j, ++t) {
         const int s = t % C::NS;
         const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / C::NS) & 1, p.err));
         const uint32_t kbase = smem_base + s * C::STAGE_BYTES;
         // partial S over this warp's k-steps w + 4i (dims 64i + 16w .. +15, i = 0..8): 16 heads
-        // x 16 tokens as two 8-token n-tiles, even and odd i in separate accumulators
-        uint64_t sp[2][2][2];  // [chain][n-tile][row half] packed column pairs
+        // x 16 tokens as two 8-token n-tiles, even and odd i in separate accumulators; stored
+        // by row: xs[w][row][token] (rows 24 floats apart: the stores meet no bank twice)
         {
           float acc[2][2][4] = {};
           if (got) {
@@ -253,129 +259,71 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
               mma_16816(acc[i & 1][1], qa, b2r, b3r);
             }
           }
+          float* xw = xch + w * (16 * 24);
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              sp[c2][nt][0] = sm::f2(acc[c2][nt][0], acc[c2][nt][1]);
-              sp[c2][nt][1] = sm::f2(acc[c2][nt][2], acc[c2][nt][3]);
-            }
+            for (int h = 0; h < 2; ++h)
+              *reinterpret_cast<float2*>(xw + (r0 + 8 * h) * 24 + nt * 8 + tok0) =
+                  make_float2(acc[0][nt][2 * h] + acc[1][nt][2 * h], acc[0][nt][2 * h + 1] + acc[1][nt][2 * h + 1]);
         }
-        // the four warps' partial tiles, summed in the same order by every warp; buffer t & 1,
-        // laid out [warp][n-tile][lane][4] so that each quarter-warp stores 128 contiguous bytes
-        {
-          ulonglong2* xw = reinterpret_cast<ulonglong2*>(xch + ((t & 1) * C::NCW + w) * 256);
-          xw[lane] = make_ulonglong2(sm::add2(sp[0][0][0], sp[1][0][0]), sm::add2(sp[0][0][1], sp[1][0][1]));
-          xw[32 + lane] = make_ulonglong2(sm::add2(sp[0][1][0], sp[1][1][0]), sm::add2(sp[0][1][1], sp[1][1][1]));
-        }
-        if (lane == 0) s_gave_up[t & 1][w] = got ? 0 : 1;
+        if (lane == 0) s_gave_up[w] = got ? 0 : 1;
         compute_bar();
-        // every warp takes the same decision from the same four flags (buffer t & 1 is not
-        // rewritten before all four have passed the next barrier)
-        if (s_gave_up[t & 1][0] | s_gave_up[t & 1][1] | s_gave_up[t & 1][2] | s_gave_up[t & 1][3]) {
+        if (s_gave_up[0] | s_gave_up[1] | s_gave_up[2] | s_gave_up[3]) {
           if (lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
           ok = false;
           break;
         }
-        uint64_t sc[2][2];  // [n-tile][row half]: columns tok0, tok0 + 1 (+ 8 for n-tile 1)
+        // row R's scores at tokens T, T + 1: the four partials summed in a fixed order
+        float s0, s1;
         {
-          // this warp's own partial comes from registers (same values, same order of sums)
-          const ulonglong2* xb = reinterpret_cast<const ulonglong2*>(xch + (t & 1) * C::NCW * 256);
-          const uint64_t own[2][2] = {{sm::add2(sp[0][0][0], sp[1][0][0]), sm::add2(sp[0][0][1], sp[1][0][1])},
-                                      {sm::add2(sp[0][1][0], sp[1][1][0]), sm::add2(sp[0][1][1], sp[1][1][1])}};
-#pragma unroll
-          for (int u = 0; u < C::NCW; ++u) {
-            uint64_t x[2][2];
-            if (u == w) {
-              x[0][0] = own[0][0];
-              x[0][1] = own[0][1];
-              x[1][0] = own[1][0];
-              x[1][1] = own[1][1];
-            } else {
-              const ulonglong2 a = xb[u * 64 + lane], b = xb[u * 64 + 32 + lane];
-              x[0][0] = a.x;
-              x[0][1] = a.y;
-              x[1][0] = b.x;
-              x[1][1] = b.y;
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) sc[nt][hh] = u == 0 ? x[nt][hh] : sm::add2(sc[nt][hh], x[nt][hh]);
-          }
-        }
-        float f[2][4];  // unpacked scores: f[nt][2h + c], row r0 + 8h, token nt*8 + tok0 + c
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          sm::unf2(sc[nt][0], f[nt][0], f[nt][1]);
-          sm::unf2(sc[nt][1], f[nt][2], f[nt][3]);
+          const float2 x0 = *reinterpret_cast<const float2*>(xch + (0 * 16 + srow) * 24 + stok);
+          const float2 x1 = *reinterpret_cast<const float2*>(xch + (1 * 16 + srow) * 24 + stok);
+          const float2 x2 = *reinterpret_cast<const float2*>(xch + (2 * 16 + srow) * 24 + stok);
+          const float2 x3 = *reinterpret_cast<const float2*>(xch + (3 * 16 + srow) * 24 + stok);
+          s0 = ((x0.x + x1.x) + x2.x) + x3.x;
+          s1 = ((x0.y + x1.y) + x2.y) + x3.y;
         }
         const int valid = min(C::BS, ctx - j * C::BS);  // tokens of this block
+        if (stok >= valid) s0 = -CUDART_INF_F;
+        if (stok + 1 >= valid) s1 = -CUDART_INF_F;
+        // online softmax in log2 units for row R
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float m_new = fmaxf(m_row, mx * p.scale_log2);
+        const float alpha = ex2_approx(m_row - m_new);  // 1 when the max holds; 0 on the first block
+        m_row = m_new;
+        const float p0 = ex2_approx(fmaf(s0, p.scale_log2, -m_new)), p1 = ex2_approx(fmaf(s1, p.scale_log2, -m_new));
+        l_lane = fmaf(l_lane, alpha, p0 + p1);
+        *reinterpret_cast<uint32_t*>(sP + srow * 48 + stok * 2) = pack_bf16(p0, p1);
+        if ((lane & 7) == 0) s_alpha[srow] = alpha;
+        const bool grow = __any_sync(0xffffffffu, alpha != 1.f);
+        if (lane == 0) s_grow[w] = grow ? 1 : 0;
         if (valid < C::BS) {
-          // zero this warp's value rows past the end (its two boxes: the other warps are past
-          // the barrier and read only their own boxes), so that P = 0 meets no non-finite value
+          // zero this warp's value rows past the end (its two boxes: every warp finished
+          // reading this stage's keys before the barrier), so that P = 0 meets no non-finite
+          // value
           uint8_t* sK = smem + s * C::STAGE_BYTES;
           for (int c2 = lane; c2 < (C::BS - valid) * 16; c2 += 32) {
             const int rrow = valid + c2 / 16, rest = c2 % 16;
             *reinterpret_cast<uint4*>(sK + (2 * w + rest / 8) * 2048 + rrow * 128 + (rest % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
-          __syncwarp();
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (nt * 8 + tok0 + (e & 1) >= valid) f[nt][e] = -CUDART_INF_F;
         }
-        // online softmax in log2 units (identical state in all four warps); O and l are
-        // rescaled only when a row's running max grows (the factor is exactly 1 otherwise)
-        float m_new[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float mx = sm::max3(f[0][2 * h], f[0][2 * h + 1], fmaxf(f[1][2 * h], f[1][2 * h + 1]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          m_new[h] = fmaxf(m_run[h], mx * p.scale_log2);
-        }
-        if (__any_sync(0xffffffffu, m_new[0] > m_run[0] || m_new[1] > m_run[1])) {
-          float alpha[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            alpha[h] = ex2_approx(m_run[h] - m_new[h]);  // 0 on the first block (m_run = -inf)
-            l_run[h] *= alpha[h];
-            m_run[h] = m_new[h];
-          }
+        compute_bar();
+        // P (16 heads x 16 tokens, bf16) as the A fragment; O rescaled only when a row's max grew
+        uint32_t pa[4];
+        ldsm_x4(smem_u32(sP) + (lane & 15) * 48 + (lane >> 4) * 16, pa[0], pa[1], pa[2], pa[3]);
+        if (s_grow[0] | s_grow[1] | s_grow[2] | s_grow[3]) {
+          const float a0 = s_alpha[r0], a1 = s_alpha[r0 + 8];
 #pragma unroll
           for (int i = 0; i < C::VW / 8; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[0];
-            o[i][2] *= alpha[1];
-            o[i][3] *= alpha[1];
-          }
-        }
-        uint32_t pa[4];
-        {
-          const uint64_t sl = sm::f2(p.scale_log2, p.scale_log2);
-          const uint64_t nm0 = sm::f2(-m_run[0], -m_run[0]), nm1 = sm::f2(-m_run[1], -m_run[1]);
-          uint64_t rsum[2];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            float x[4];
-            sm::unf2(sm::fma2(sm::f2(f[nt][0], f[nt][1]), sl, nm0), x[0], x[1]);
-            sm::unf2(sm::fma2(sm::f2(f[nt][2], f[nt][3]), sl, nm1), x[2], x[3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = ex2_approx(x[e]);  // masked: 2^-inf = 0
-            const uint64_t lo = sm::f2(x[0], x[1]), hi = sm::f2(x[2], x[3]);
-            pa[2 * nt] = sm::bf16x2(lo);
-            pa[2 * nt + 1] = sm::bf16x2(hi);
-            rsum[0] = nt == 0 ? lo : sm::add2(rsum[0], lo);
-            rsum[1] = nt == 0 ? hi : sm::add2(rsum[1], hi);
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float a, b;
-            sm::unf2(rsum[h], a, b);
-            l_run[h] += a + b;
+            o[i][0] *= a0;
+            o[i][1] *= a0;
+            o[i][2] *= a1;
+            o[i][3] *= a1;
           }
         }
         // O += P V over this warp's 128 value dims (boxes 2w and 2w + 1 of the same rows)
@@ -399,12 +347,19 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 2) mla_decode_kernel(const De
         Piece np;
         if (nx.next(np)) request_q(s_row[np.i]);
       }
-      // ---- the piece's result for this warp's slice ----
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+      // ---- the piece's result for this warp's slice: rows r0 and r0 + 8 of every warp's
+      // softmax state, through shared memory ----
+      l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 1);
+      l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 2);
+      l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 4);
+      if ((lane & 7) == 0) {
+        s_lm[srow][0] = m_row;
+        s_lm[srow][1] = l_lane;
       }
+      compute_bar();
+      const float m_run[2] = {s_lm[r0][0], s_lm[r0 + 8][0]};
+      const float l_run[2] = {s_lm[r0][1], s_lm[r0 + 8][1]};
+      compute_bar();  // s_lm is rewritten at the next piece end only after every warp read it
       const int unit_blocks = (ctx + C::BS - 1) / C::BS;
       const bool whole = pc.lo == 0 && pc.hi == unit_blocks;
       float inv[2], lse[2];

@@ -129,19 +129,29 @@ def load_peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "source": "fallback"}
 
 
-def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "paged_kv_attention_reshape_gb300", "csrc", name)
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+# The source files each profiled kernel is compiled from (its .cu and the headers it includes).
+KERNEL_SOURCES = {
+    "paged_decode": ["decode.cu", "decode_shares.cuh", "common.cuh", "launch.h"],
+    "mla_decode": ["mla_decode.cu", "decode_shares.cuh", "common.cuh", "softmax.cuh", "launch.h"],
+}
 
 
-def profiled_traffic(kernel_file: str, key: str):
+def kernel_source_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_reshape_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, key: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
     source of the kernel; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t[key]
-        if e.get("source_sha") != kernel_source_hash(kernel_file):
+        if e.get("source_sha") != kernel_source_hash(KERNEL_SOURCES[kernel]):
             return None
         return e["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
@@ -664,7 +674,7 @@ def main():
     value = replica_rate(w["kv_bytes"], ws, step_ms) / 1e9
     dec_ms = sum(sec["decode"]) / len(sec["decode"])   # mean over the decode-alone launches
     achieved = w["alg_bytes"] / (dec_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("decode.cu", "paged_decode_qwen3")
+    traffic = profiled_traffic("paged_decode", "paged_decode_qwen3")
     if ws > 1:
         torch.distributed.barrier()
     e2e_ms, h2d, d2h = bench_decode_e2e(pkv, w, dev, stream, steps, warmup, timer)
@@ -746,6 +756,8 @@ def main():
                 "launch_ms": r["launch_ms"],
                 "roofline_frac": r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"],
                 "mma_tflops": r["flops"] / (r["launch_ms"] * 1e-3) / 1e12,
+                "traffic": profiled_traffic("mla_decode", "mla_deepseek_tp8"),
+                "algorithmic_bytes_per_launch": r["alg_bytes"],
                 "device_errors": r["errors"],
             }
         except Exception as e:

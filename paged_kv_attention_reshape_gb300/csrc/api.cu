@@ -430,6 +430,8 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
   p.G = 16;                            // query heads per group
   p.units = num_q_heads / 16 * 4;      // four 128-wide value slices per group
   p.out_dim = v_dim;
+  p.kv = cache.k;
+  p.kv_block_bytes = cache.stride_block * 2;
   p.num_blocks = cache.num_blocks;
   p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -37,6 +37,8 @@ struct DecodeParams {
   // the MLA decode one per slice of the value dims of a group of G query heads (out_dim = the
   // value width).
   int32_t units, out_dim;
+  const void* kv;           // MLA decode: the latent cache (blocks kv_block_bytes apart)
+  int64_t kv_block_bytes;
 };
 
 // Extend and prefill share one kernel; prefill is the case without cached context.

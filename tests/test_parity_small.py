@@ -351,7 +351,7 @@ def test_decode_edge_lengths_and_splits(pkv, ctxs):
 @pytest.mark.parametrize("ctxs", [[256], [640], [2048], [2176], [8320], [80000], [192000], [50000, 7, 30000]])
 def test_decode_long_sequences_merge_tree(pkv, ctxs):
     """A few long sequences spread over all the CTAs: each is cut into up to one piece per
-    share, and the pieces are merged along the fan-in-4 tree (depths 1 to 6 here, including
+    share, and the pieces are merged along the fan-in-4 tree (depths 1 to 5 here, including
     partly filled groups)."""
     b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=1, D=128, seed=sum(ctxs) % 101)
     g = b.to(DEV)

@@ -89,49 +89,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
   }
   if (n > C::MAXR) n = C::MAXR;
   const int cap = min(p.max_seq_len, p.max_blocks * C::BS);
-  int carry = 0;
-  for (int base = 0; base < n; base += nthreads) {
-    const int i = base + tid;
-    int cnt = 0;
-    if (i < n) {
-      const int r = p.order ? p.order[begin + i] : begin + i;
-      int ctx = 0;
-      if (r >= 0 && r < p.batch_reqs) {
-        ctx = p.seq_lens[r];
-        if (ctx > cap) {
-          if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_LEN);
-          ctx = cap;
-        }
-        ctx = max(ctx, 0);
-        s_row[i] = p.cu_q ? p.cu_q[r] : r;
-        s_r[i] = r;
-      } else {
-        if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_REQS);
-        s_r[i] = -1;
-        s_row[i] = 0;
-      }
-      s_ctx[i] = ctx;
-      cnt = (ctx + C::BS - 1) / C::BS;
-    }
-    int x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_scan[warp] = x;
-    __syncthreads();
-    int wprefix = 0, tot = 0;
-    for (int w = 0; w < nw; ++w) {
-      if (w < warp) wprefix += s_scan[w];
-      tot += s_scan[w];
-    }
-    if (i < n) s_pre[i] = carry + wprefix + x - cnt;
-    carry += tot;
-    __syncthreads();
-  }
-  if (tid == 0) s_pre[n] = carry;
-  __syncthreads();
+  const int carry = static_cast<int>(scan_set<C::BS>(p.order, p.seq_lens, p.cu_q, begin, n, p.batch_reqs, cap,
+                                                     p.err, s_pre, s_ctx, s_r, s_row, s_scan));
   const int64_t TB = carry;
   if (blockIdx.x == 0 && blockIdx.y == 0) {
     // sequences with no context: out = 0, lse = -inf (no share covers them)

@@ -36,65 +36,84 @@ __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, i
 }
 
 // The set's sequences into shared memory (every CTA, redundantly): per position i < n, the
-// request s_r[i] (-1 if out of range), its query row s_row[i], its context length s_ctx[i]
-// (cut to max_seq_len and the table, flagged), and the exclusive prefix s_pre[i] of the
-// 16-token block counts (s_pre[n] = the total, returned). CTA (0, 0) also writes out = 0 and
-// lse = -inf for the sequences with no context, which no share covers. All threads of the
-// CTA call it; s_scan holds one int per warp.
-template <int MAXR, int BS>
-__device__ __forceinline__ int64_t load_set(const DecodeParams& p, int begin, int& n, int* s_pre, int* s_ctx, int* s_r,
-                            int* s_row, int* s_scan) {
+// request s_r[i] (-1 if out of range, flagged), its query row s_row[i], its context length
+// s_ctx[i] (cut to `cap` tokens, flagged), and the exclusive prefix s_pre[i] of the BS-token
+// block counts (s_pre[n] = the total, returned). The loads of all positions are issued before
+// any is waited for (two dependent rounds: the order, then lengths and rows), and the prefix
+// is one block-wide scan. All threads of the CTA call it; s_scan holds one int per warp.
+// Kept out of line: it runs once per CTA, and the streaming loop after it keeps its registers.
+template <int BS>
+__device__ __noinline__ int64_t scan_set(const int32_t* order, const int32_t* seq_lens, const int32_t* cu_q,
+                                         int begin, int n, int batch_reqs, int cap, unsigned int* err, int* s_pre,
+                                         int* s_ctx, int* s_r, int* s_row, int* s_scan) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nw = nthreads >> 5;
+  const bool report = blockIdx.x == 0 && blockIdx.y == 0;
+#pragma unroll 4
+  for (int i = tid; i < n; i += nthreads) s_r[i] = order ? order[begin + i] : begin + i;
+#pragma unroll 4
+  for (int i = tid; i < n; i += nthreads) {  // the same positions as above: no barrier needed
+    const int r = s_r[i];
+    int ctx = 0, row = 0;
+    if (r >= 0 && r < batch_reqs) {
+      ctx = seq_lens[r];
+      row = cu_q ? cu_q[r] : r;
+      if (ctx > cap) {
+        if (report) flag_error(err, PKV_DEVERR_LEN);
+        ctx = cap;
+      }
+      ctx = max(ctx, 0);
+    } else {
+      if (report) flag_error(err, PKV_DEVERR_REQS);
+      s_r[i] = -1;
+    }
+    s_ctx[i] = ctx;
+    s_row[i] = row;
+    s_pre[i] = (ctx + BS - 1) / BS;
+  }
+  __syncthreads();
+  // exclusive scan of the block counts: each thread a contiguous segment
+  const int seg = (n + nthreads - 1) / nthreads;
+  const int lo = min(n, tid * seg), hi = min(n, lo + seg);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += s_pre[i];
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  __syncthreads();
+  int run = x - sum, total = 0;
+  for (int w = 0; w < nw; ++w) {
+    if (w < warp) run += s_scan[w];
+    total += s_scan[w];
+  }
+  for (int i = lo; i < hi; ++i) {
+    const int c = s_pre[i];
+    s_pre[i] = run;
+    run += c;
+  }
+  if (tid == 0) s_pre[n] = total;
+  __syncthreads();
+  return total;
+}
+
+// The set's sequences into shared memory (scan_set), the set's size checks, and out = 0,
+// lse = -inf for the sequences with no context, which no share covers (CTA (0, 0)).
+template <int MAXR, int BS>
+__device__ __forceinline__ int64_t load_set(const DecodeParams& p, int begin, int& n, int* s_pre, int* s_ctx, int* s_r,
+                                            int* s_row, int* s_scan) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
     if (p.bounds != nullptr && p.bounds[p.cls + 1] - p.bounds[p.cls] > p.max_reqs) flag_error(p.err, PKV_DEVERR_REQS);
     if (n > MAXR) flag_error(p.err, PKV_DEVERR_REQS);
   }
   if (n > MAXR) n = MAXR;
   const int cap = min(p.max_seq_len, p.max_blocks * BS);
-  int carry = 0;
-  for (int base = 0; base < n; base += nthreads) {
-    const int i = base + tid;
-    int cnt = 0;
-    if (i < n) {
-      const int r = p.order ? p.order[begin + i] : begin + i;
-      int ctx = 0;
-      if (r >= 0 && r < p.batch_reqs) {
-        ctx = p.seq_lens[r];
-        if (ctx > cap) {
-          if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_LEN);
-          ctx = cap;
-        }
-        ctx = max(ctx, 0);
-        s_row[i] = p.cu_q ? p.cu_q[r] : r;
-        s_r[i] = r;
-      } else {
-        if (blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_REQS);
-        s_r[i] = -1;
-        s_row[i] = 0;
-      }
-      s_ctx[i] = ctx;
-      cnt = (ctx + BS - 1) / BS;
-    }
-    int x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_scan[warp] = x;
-    __syncthreads();
-    int wprefix = 0, tot = 0;
-    for (int w = 0; w < nw; ++w) {
-      if (w < warp) wprefix += s_scan[w];
-      tot += s_scan[w];
-    }
-    if (i < n) s_pre[i] = carry + wprefix + x - cnt;
-    carry += tot;
-    __syncthreads();
-  }
-  if (tid == 0) s_pre[n] = carry;
-  __syncthreads();
+  const int64_t total = scan_set<BS>(p.order, p.seq_lens, p.cu_q, begin, n, p.batch_reqs, cap, p.err, s_pre, s_ctx,
+                                     s_r, s_row, s_scan);
   if (blockIdx.x == 0 && blockIdx.y == 0) {
     for (int i = tid; i < n; i += nthreads) {
       if (s_ctx[i] != 0 || s_r[i] < 0) continue;
@@ -105,7 +124,7 @@ __device__ __forceinline__ int64_t load_set(const DecodeParams& p, int begin, in
         for (int h = 0; h < p.Hq; ++h) p.lse[row * p.Hq + h] = -CUDART_INF_F;
     }
   }
-  return carry;
+  return total;
 }
 
 // Balanced partition of TB blocks into nsh shares: share w holds base + (w < rem) blocks.

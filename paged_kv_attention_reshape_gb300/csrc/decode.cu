@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
 
   // ---- cut sequences: their pieces' partials and the merge tree ----
   __shared__ CutState s_cut[C::MAXW];
-  CutMerger<D, 1, D> merger(&s_cut[warp], lane);
+  CutMerger<D, 1, D, FP8> merger(&s_cut[warp], lane);
 
   // ---- compute cursor ----
   Piece pc;
@@ -229,18 +229,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
     cp_async_wait_all();
     __syncwarp();
     uint32_t qa[D / 16][4];
-    {
+    if constexpr (FP8) {
+      // The FP8 path multiplies in fp16 (E4M3 codes convert to it exactly). Its key fragments
+      // come from ldmatrix on the code rows, which hands lane l the four codes of dims
+      // 16 ks + 4 (l % 4) .. + 3: so the MMA's k = 2 (l % 4) + {0, 1} and + {8, 9} stand for
+      // those four dims, and the query fragment takes the same four dims (one 8-byte load
+      // per row and k-step). The dot product sums the same pairs.
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int chunk = 2 * ks + ((lane & 3) >> 1);  // 16-byte chunk of dims 16 ks + 4 (lane % 4)
+          const uint2 v = *reinterpret_cast<const uint2*>(sQ + (chunk / 8) * 2048 +
+                                                          sw128(r0 + 8 * h, chunk % 8) + (lane & 1) * 8);
+          qa[ks][h] = bf16x2_to_f16x2(v.x);
+          qa[ks][2 + h] = bf16x2_to_f16x2(v.y);
+        }
+    } else {
       const uint32_t qbase = smem_u32(sQ);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         ldsm_x4(qbase + (ks / 4) * 2048 + sw128(lane & 15, (ks % 4) * 2 + (lane >> 4)), qa[ks][0], qa[ks][1],
                 qa[ks][2], qa[ks][3]);
-      if constexpr (FP8) {  // the FP8 path multiplies in fp16: E4M3 codes convert to it exactly
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) qa[ks][i] = bf16x2_to_f16x2(qa[ks][i]);
-      }
     }
     __syncwarp();
     {
@@ -276,19 +286,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
       // S = Q K^T : 16 rows x 16 tokens as two 8-token n-tiles
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       if constexpr (FP8) {
-        // B fragment of token n = 8 nt + lane/4, dims 16 ks + 2 (lane % 4) + {0, 1} (+ 8): two
-        // code pairs of the token's 128-byte row (16-byte chunk ks, swizzled by the row)
+        // B fragments, two k-steps per ldmatrix.x4: matrix m holds tokens 8 (m % 2) .. + 7 and
+        // the 16 codes of chunk ks + m / 2 (one 16-byte chunk of each 128-byte row, swizzled
+        // by the row); lane l gets token 8 (m % 2) + l / 4, dims 4 (l % 4) .. + 3 of the chunk
+        const uint32_t kbase = smem_u32(sK);
+        const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int tok = nt * 8 + (lane >> 2);
-          const uint8_t* rowp = sK + tok * 128 + 2 * (lane & 3);
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          uint32_t r[4];
+          ldsm_x4(kbase + tok * 128 + (((ks + (lane >> 4)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint8_t* cp = rowp + ((ks ^ (tok & 7)) << 4);
-            const uint32_t b0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(cp));
-            const uint32_t b1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(cp + 8));
-            mma_16816_f16(sc[nt], qa[ks], b0, b1);
-          }
+          for (int m = 0; m < 4; ++m)
+            mma_16816_f16(sc[m & 1], qa[ks + (m >> 1)], e4m3x2_to_f16x2(static_cast<uint16_t>(r[m])),
+                          e4m3x2_to_f16x2(static_cast<uint16_t>(r[m] >> 16)));
         }
       } else {
         const uint32_t kbase = smem_u32(sK);
@@ -347,16 +357,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
         pa[1] = pack_f16(sc[0][2], sc[0][3]);
         pa[2] = pack_f16(sc[1][0], sc[1][1]);
         pa[3] = pack_f16(sc[1][2], sc[1][3]);
-        // O += P V: the B fragment of dim n = 8 nt + lane/4 holds tokens 2 (lane % 4) + {0, 1}
-        // (+ 8): four codes from four token rows, paired and converted to fp16
-        const int t0 = 2 * (lane & 3);
+        // O += P V. ldmatrix.trans of the code rows, two 16-dim groups per x4: matrix m holds
+        // tokens 8 (m % 2) .. + 7 and chunk g + m / 2; lane l gets, of tokens 2 (l % 4) and
+        // + 1, the codes of dims 2 (l / 4) and + 1 of the group. Bytes 0 and 2 pair into the
+        // B fragment of n-tile 2g (the group's even dims), bytes 1 and 3 into n-tile 2g + 1
+        // (its odd dims): O holds the dims in that order (out_dim_of with VPERM).
+        const uint32_t vbase = smem_u32(sV);
+        const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          const int n = nt * 8 + (lane >> 2);
-          auto code = [&](int tok) { return static_cast<uint32_t>(sV[tok * 128 + (((n >> 4) ^ (tok & 7)) << 4) + (n & 15)]); };
-          const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(code(t0) | (code(t0 + 1) << 8)));
-          const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(code(t0 + 8) | (code(t0 + 9) << 8)));
-          mma_16816_f16(o[nt], pa, b0, b1);
+        for (int g = 0; g < D / 16; g += 2) {
+          uint32_t r[4];
+          ldsm_x4_t(vbase + tok * 128 + (((g + (lane >> 4)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int gg2 = 0; gg2 < 2; ++gg2) {
+            const uint32_t lo = r[2 * gg2], hi = r[2 * gg2 + 1];  // tokens 2 (l % 4) + {0, 1}, + 8
+            mma_16816_f16(o[2 * (g + gg2)], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(lo, 0, 0x20))),
+                          e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(hi, 0, 0x20))));
+            mma_16816_f16(o[2 * (g + gg2) + 1], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(lo, 0, 0x31))),
+                          e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(hi, 0, 0x31))));
+          }
         }
       } else {
         pa[0] = pack_bf16(sc[0][0], sc[0][1]);
@@ -403,9 +422,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
         if (gg >= G) continue;
         const int hq = kh * G + gg;
         __nv_bfloat16* dst = p.out + (row * p.Hq + hq) * D + 2 * (lane & 3);
+        if constexpr (FP8) {  // n-tiles 2g / 2g + 1 hold the even / odd dims of group g
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-          *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+          for (int g = 0; g < D / 16; ++g)
+            *reinterpret_cast<uint2*>(dst + 16 * g + 2 * (lane & 3)) =
+                make_uint2(pack_bf16(o[2 * g][2 * h] * inv[h], o[2 * g + 1][2 * h] * inv[h]),
+                           pack_bf16(o[2 * g][2 * h + 1] * inv[h], o[2 * g + 1][2 * h + 1] * inv[h]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i)
+            *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+        }
         if (p.lse && (lane & 3) == 0) p.lse[row * p.Hq + hq] = lse[h];
       }
       continue;

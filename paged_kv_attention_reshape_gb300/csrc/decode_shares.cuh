@@ -298,8 +298,17 @@ __device__ __forceinline__ void fold_siblings(const DecodeParams& p, const Cut& 
   }
 }
 
+// Output dims of the accumulator layout. Without VPERM, column c of n-tile i is dim i*8 + c.
+// With VPERM (the FP8 decode, whose value fragments come from a transposed ldmatrix of
+// byte codes), n-tiles 2g and 2g + 1 hold the even and the odd dims of the 16-dim group g:
+// column c of n-tile i is dim 16 (i / 2) + 2c + (i % 2).
+template <int D, bool VPERM>
+__device__ __forceinline__ int out_dim_of(int i, int c) {
+  return VPERM ? 16 * (i >> 1) + 2 * c + (i & 1) : i * 8 + c;
+}
+
 // out/lse of the cut sequence from registers (the merge's root).
-template <int D, int UPG, int OUT_DIM>
+template <int D, int UPG, int OUT_DIM, bool VPERM = false>
 __device__ __forceinline__ void write_out_regs(const DecodeParams& p, const Cut& s, int kh, float (&o)[D / 8][4], float (&lse)[2],
                                                int lane) {
   const int r0 = lane >> 2, col = 2 * (lane & 3);
@@ -307,10 +316,18 @@ __device__ __forceinline__ void write_out_regs(const DecodeParams& p, const Cut&
   for (int h = 0; h < 2; ++h) {
     const int gg = r0 + 8 * h;
     if (gg >= p.G) continue;
-    __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg) + col;
+    __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg);
+    if constexpr (VPERM) {
+      // dims 16g + 2col + {0, 1, 2, 3}: columns col, col + 1 of n-tiles 2g (even) and 2g + 1 (odd)
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-      *reinterpret_cast<uint32_t*>(dst + i * 8) = pack_bf16(o[i][2 * h], o[i][2 * h + 1]);
+      for (int g = 0; g < D / 16; ++g)
+        *reinterpret_cast<uint2*>(dst + 16 * g + 2 * col) =
+            make_uint2(pack_bf16(o[2 * g][2 * h], o[2 * g + 1][2 * h]), pack_bf16(o[2 * g][2 * h + 1], o[2 * g + 1][2 * h + 1]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<uint32_t*>(dst + i * 8 + col) = pack_bf16(o[i][2 * h], o[i][2 * h + 1]);
+    }
     if (p.lse && (lane & 3) == 0 && kh % UPG == 0) p.lse[s.row * p.Hq + out_head<UPG>(p, kh, gg)] = lse[h];
   }
 }
@@ -337,7 +354,7 @@ __device__ __forceinline__ void store_regs(const DecodeParams& p, const Cut& s, 
 // heads at a time, every lane loads its elements l*PER .. l*PER+PER-1 of all children before
 // folding them, so each group costs one round trip to L2 (the partials were written by other
 // SMs and are read from L2).
-template <int D, int UPG, int OUT_DIM>
+template <int D, int UPG, int OUT_DIM, bool VPERM = false>
 __device__ __forceinline__ void merge_node(const DecodeParams& p, const Cut& s, int L, int a, int k, bool root,
                                            int kh, int lane) {
   constexpr int PER = D / 32;
@@ -397,9 +414,17 @@ __device__ __forceinline__ void merge_node(const DecodeParams& p, const Cut& s, 
       if (gg >= G) continue;
       const float lse = Wg > 0.f ? Mg + __logf(Wg) : -CUDART_INF_F;
       if (root) {
-        __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg) + lane * PER;
+        __nv_bfloat16* dst = p.out + out_offset<D, UPG, OUT_DIM>(p, s.row, kh, gg);
+        if constexpr (VPERM) {
 #pragma unroll
-        for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e], acc[e + 1]);
+          for (int e = 0; e < PER; ++e) {
+            const int l = lane * PER + e;  // accumulator-layout dim: n-tile l / 8, column l % 8
+            dst[out_dim_of<D, true>(l >> 3, l & 7)] = __float2bfloat16_rn(acc[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + lane * PER + e) = pack_bf16(acc[e], acc[e + 1]);
+        }
         if (p.lse && lane == 0 && kh % UPG == 0) p.lse[s.row * p.Hq + out_head<UPG>(p, kh, gg)] = lse;
       } else {
         float* dst = node_part<D>(p, s, L, a, kh, gg);
@@ -426,7 +451,7 @@ struct CutState {
 // The merge work of one warp for one unit kh: finished cut pieces enter the tree, arrivals are
 // deferred by one block (so that the stores before them have drained), and the merges they
 // complete run when the warp's share is done.
-template <int D, int UPG, int OUT_DIM>
+template <int D, int UPG, int OUT_DIM, bool VPERM = false>
 struct CutMerger {
   CutState* st;       // this warp's state (shared memory)
   bool pend = false;  // an arrival is owed
@@ -469,7 +494,7 @@ struct CutMerger {
         check = true;  // the siblings were in: the next level is likely complete too
       }
       if (s.nodes(L) == 1) {
-        write_out_regs<D, UPG, OUT_DIM>(p, s, kh, o, lse, lane);
+        write_out_regs<D, UPG, OUT_DIM, VPERM>(p, s, kh, o, lse, lane);
         return;
       }
       ai = a;
@@ -512,7 +537,7 @@ struct CutMerger {
       int L = st->due_L[d], a = st->due_a[d];
       for (;;) {
         const bool root = s.nodes(L) == 1;
-        merge_node<D, UPG, OUT_DIM>(p, s, L, a, s.children(L, a), root, kh, lane);
+        merge_node<D, UPG, OUT_DIM, VPERM>(p, s, L, a, s.children(L, a), root, kh, lane);
         if (root) break;
         // the parent with more than one child (a lone child is its parent)
         int k;

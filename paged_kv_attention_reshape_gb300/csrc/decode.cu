@@ -40,12 +40,15 @@
 namespace pkv {
 
 // FP8: the cache holds E4M3 codes (one byte per element). A block row of one head is then
-// D bytes (one 128-byte TMA box at D = 128), a stage half as large, and twice as many stages
-// keep the same bytes in flight per warp in the same shared memory.
+// D bytes (one 128-byte TMA box at D = 128) and a stage half as large; the smaller rings let
+// three CTAs share an SM (12 warps instead of 8, at most 168 registers each), which the
+// conversions of the codes need to keep the stream going.
 template <int D, bool FP8 = false>
 struct DecodeCfg {
   static constexpr int MAXW = 8;                      // warps (KV heads) per CTA, at most
-  static constexpr int NSW = FP8 ? 4 : 2;             // ring stages per warp
+  static constexpr int NSW = 2;                       // ring stages per warp
+  static constexpr int WARPS_PER_SM = FP8 ? 12 : 8;   // resident warps per SM the launch aims for
+  static constexpr int MAXREG = FP8 ? 168 : 255;      // registers per thread (12 warps per SM fit)
   static constexpr int BS = 16;                       // tokens per block
   static constexpr int EB = FP8 ? 1 : 2;              // bytes per cached element
   static constexpr int HALVES = FP8 ? 1 : D / 64;     // 128-byte column boxes per row
@@ -61,7 +64,7 @@ struct DecodeCfg {
 };
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_kernel(
+__global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) __maxnreg__((DecodeCfg<D, FP8>::MAXREG)) paged_decode_kernel(
     const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
   using C = DecodeCfg<D, FP8>;
@@ -464,33 +467,40 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) paged_decode_ker
 // block, less room for the kernel's few static shared variables.
 static int max_dyn_smem() { return max_smem_optin() - 1024; }
 
-static_assert(DecodeCfg<128, true>::WARP_BYTES == DecodeCfg<128>::WARP_BYTES,
-              "the FP8 and bf16 decode take the same launch shape");
-// Launch shape: warps per CTA = KV heads per CTA (at most 8); about 8 warps per SM.
+// Launch shape: warps per CTA = KV heads per CTA (at most 8); about WARPS_PER_SM warps per SM,
+// as many CTAs as shared memory allows.
 struct DecodeShape {
   int nw, groups, shares;
 };
+template <int D, bool FP8>
 static DecodeShape decode_shape(int Hkv) {
+  using C = DecodeCfg<D, FP8>;
   DecodeShape d;
-  d.nw = Hkv < DecodeCfg<128>::MAXW ? Hkv : DecodeCfg<128>::MAXW;
-  while (d.nw > 1 && DecodeCfg<128>::smem(d.nw) > max_dyn_smem()) --d.nw;
+  d.nw = Hkv < C::MAXW ? Hkv : C::MAXW;
+  while (d.nw > 1 && C::smem(d.nw) > max_dyn_smem()) --d.nw;
   d.groups = (Hkv + d.nw - 1) / d.nw;
-  // about 8 warps per SM, as many CTAs as shared memory allows
-  int ctas_per_sm = d.nw >= 8 ? 1 : 8 / d.nw;
-  const int fit = (max_dyn_smem() + 1024) / (DecodeCfg<128>::smem(d.nw) + 1024);
+  int ctas_per_sm = C::WARPS_PER_SM / d.nw > 0 ? C::WARPS_PER_SM / d.nw : 1;
+  const int fit = (max_dyn_smem() + 1024) / (C::smem(d.nw) + 1024);
   if (ctas_per_sm > fit) ctas_per_sm = fit > 0 ? fit : 1;
   d.shares = num_sms() * ctas_per_sm / d.groups;
   if (d.shares < 1) d.shares = 1;
   return d;
 }
+// The most shares any decode launch of this head count uses (bf16 or FP8 cache).
+static int decode_max_shares(int Hkv) {
+  const int a = decode_shape<128, false>(Hkv).shares, b = decode_shape<128, true>(Hkv).shares;
+  const int c = decode_shape<64, false>(Hkv).shares;
+  return a > b ? (a > c ? a : c) : (b > c ? b : c);
+}
 
 // Workspace: partials [shares][2 slots][Hkv][G][D + 4] floats (O, then the LSE at index D; rows
-// padded to 16 bytes), then the merge-tree counters [levels][shares][2 slots][Hkv] (8 bytes each).
+// padded to 16 bytes), then the merge-tree counters [levels][shares][2 slots][Hkv] (8 bytes each),
+// for the largest share count of the head count.
 size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D) {
-  return static_cast<size_t>(decode_shape(Hkv).shares) * 2 * Hq * (D + 4) * sizeof(float);
+  return static_cast<size_t>(decode_max_shares(Hkv)) * 2 * Hq * (D + 4) * sizeof(float);
 }
 size_t decode_workspace_bytes(int Hq, int Hkv, int D) {
-  const int shares = decode_shape(Hkv).shares;
+  const int shares = decode_max_shares(Hkv);
   return decode_workspace_ctr_offset(Hq, Hkv, D) +
          static_cast<size_t>(merge_levels(shares)) * shares * 2 * Hkv * sizeof(unsigned long long);
 }
@@ -502,7 +512,7 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&paged_decode_kernel<D, FP8>), max_dyn_smem(),
                                      FP8 ? kAttrDecode128Fp8 : (D == 64 ? kAttrDecode64 : kAttrDecode128));
   if (e != cudaSuccess) return e;
-  const DecodeShape sh = decode_shape(p.Hkv);
+  const DecodeShape sh = decode_shape<D, FP8>(p.Hkv);
   e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(sh.shares, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
                  p, tk, tv);
   *launches += 1;

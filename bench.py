@@ -657,6 +657,16 @@ def profile_case(pkv, args):
         fn = lambda: pkv.paged_decode_attn(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, maxs,
                                            cu_q=b.cu_q, workspace=ws)
         what = f"decode B=64 kv_bytes={sum(b.seq_lens_list) * 4 * 128 * 4}"
+    elif args.profile == "decode_fp8":
+        # the same 64 sequences over an FP8 (E4M3) cache: ~164 MB of codes per launch
+        b = gen.decode_batch(64, 2000, 3000, Hq=64, Hkv=4, D=128, seed=1, device=dev)
+        ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+        kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+        maxs = max(b.seq_lens_list)
+        ws = torch.empty(max(16, pkv.paged_decode_workspace_size(b.R, 64, 4, 128, maxs)), dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.paged_decode_attn(b.q, kc, vc, b.block_tables, b.seq_lens, maxs, cu_q=b.cu_q,
+                                           workspace=ws, k_scale=ks, v_scale=vs)
+        what = f"decode FP8 B=64 code_bytes={sum(b.seq_lens_list) * 4 * 128 * 2}"
     elif args.profile == "mla":
         # 32 requests of the MLA workload's shape: ~390 MB of latent rows per launch
         b = gen.mla_batch(32, 10000, 11000, Hq=16, seed=5, device=dev)
@@ -697,7 +707,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["decode", "mla", "prefill", "extend", "write_pack"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mla", "prefill", "extend", "write_pack"], default=None,
                     help="run a reduced case of one kernel --steps times for an ncu capture; prints "
                          "a one-line summary, no benchmark line")
     args = ap.parse_args()

@@ -75,6 +75,9 @@ def _load():
             lib.oracle_extend.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, P, i32, i32,
                                           i32, i32, f64, P, P, P, i32]
             lib.oracle_extend.restype = None
+            lib.oracle_extend_fp8.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, P, i32, i32, i32, i32,
+                                              f64, f64, f64, P, P, i32]
+            lib.oracle_extend_fp8.restype = None
             lib.oracle_extend_chunked.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, i32,
                                                   i32, i32, i32, f64, i64, P, P]
             lib.oracle_extend_chunked.restype = None
@@ -315,6 +318,30 @@ def extend(q, k_new, v_new, cu_q, scale, seq_lens=None, k_cache=None, v_cache=No
 def prefill(q, k, v, cu_seqlens, scale, req_ids=None, n_req=None, row_mask=None, nthreads=None):
     return extend(q, k, v, cu_seqlens, scale, req_ids=req_ids, n_req=n_req, row_mask=row_mask,
                   nthreads=nthreads)
+
+
+def extend_fp8(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, scale, k_scale, v_scale,
+               req_ids=None, n_req=None, nthreads=None, out=None, lse=None):
+    """Extend over an FP8 cache: k_cache / v_cache uint8 E4M3 codes [nb, bs, Hkv, D] standing for
+    e4m3(code) * k_scale / v_scale; new tokens bf16 bits. Returns (out, lse) float64."""
+    lib = _load()
+    q, k_new, v_new = _c(q, np.uint16), _c(k_new, np.uint16), _c(v_new, np.uint16)
+    cu_q, seq_lens, req_ids = _c(cu_q, np.int32), _c(seq_lens, np.int32), _c(req_ids, np.int32)
+    k_cache, v_cache = _c(k_cache, np.uint8), _c(v_cache, np.uint8)
+    block_tables = _c(block_tables, np.int32)
+    T, Hq, D = q.shape
+    hkv = k_new.shape[1]
+    if n_req is None:
+        n_req = req_ids.shape[0] if req_ids is not None else cu_q.shape[0] - 1
+    if out is None:
+        out = np.full((T, Hq, D), np.nan)
+    if lse is None:
+        lse = np.full((T, Hq), np.nan)
+    lib.oracle_extend_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(seq_lens), _ptr(k_cache),
+                          _ptr(v_cache), k_cache.shape[0], k_cache.shape[1], _ptr(block_tables),
+                          block_tables.shape[1], _ptr(req_ids), n_req, Hq, hkv, D, float(scale), float(k_scale),
+                          float(v_scale), _ptr(out), _ptr(lse), nthreads or default_threads())
+    return out, lse
 
 
 def extend_chunked(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, scale,

@@ -564,6 +564,49 @@ void oracle_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const ui
   });
 }
 
+// Extend over an FP8 (E4M3) cache ([ROCm-attn] MLA section: the cached context is gathered
+// and dequantised, "gather_and_maybe_dequant_cache", before the attention): the cached keys
+// and values are e4m3(code) * k_scale and e4m3(code) * v_scale; the new tokens' keys and
+// values are the bf16 rows as given. Otherwise oracle_extend.
+void oracle_extend_fp8(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                       const int32_t* cu_q, const int32_t* seq_lens, const uint8_t* k_cache,
+                       const uint8_t* v_cache, int64_t num_blocks, int32_t bs,
+                       const int32_t* block_tables, int32_t max_blocks, const int32_t* req_ids,
+                       int32_t n_req, int32_t Hq, int32_t Hkv, int32_t D, double scale, double k_scale,
+                       double v_scale, double* out, double* lse, int32_t nthreads) {
+  const Paged P{nullptr, nullptr, num_blocks, bs, Hkv, D, block_tables, max_blocks};
+  const int G = Hq / Hkv;
+  parallel_for(static_cast<int64_t>(n_req) * Hkv, nthreads, [&](int64_t item) {
+    const int64_t r = req_ids ? req_ids[item / Hkv] : item / Hkv;
+    const int kh = static_cast<int>(item % Hkv);
+    const int64_t row0 = cu_q[r], nq = cu_q[r + 1] - cu_q[r];
+    const int64_t C = std::max<int64_t>(0, seq_lens[r] - nq);
+    const int64_t nk = C + nq;
+    std::vector<double> K(static_cast<size_t>(nk) * D), V(static_cast<size_t>(nk) * D), qd(D);
+    for (int64_t j = 0; j < C; ++j) {
+      const int64_t off = paged_offset(P, r, j, kh);
+      for (int d = 0; d < D; ++d) {
+        K[j * D + d] = off < 0 ? NAN : e4m3_value(k_cache[off + d]) * k_scale;
+        V[j * D + d] = off < 0 ? NAN : e4m3_value(v_cache[off + d]) * v_scale;
+      }
+    }
+    for (int64_t j = 0; j < nq; ++j)
+      for (int d = 0; d < D; ++d) {
+        K[(C + j) * D + d] = bf16_value(k_new[((row0 + j) * Hkv + kh) * D + d]);
+        V[(C + j) * D + d] = bf16_value(v_new[((row0 + j) * Hkv + kh) * D + d]);
+      }
+    for (int64_t i = 0; i < nq; ++i) {
+      const int64_t row = row0 + i;
+      for (int g = 0; g < G; ++g) {
+        const int h = kh * G + g;
+        for (int d = 0; d < D; ++d) qd[d] = bf16_value(q[(row * Hq + h) * D + d]);
+        attend_row(qd.data(), K.data(), V.data(), C + i + 1, D, scale, out + (row * Hq + h) * D,
+                   lse + row * Hq + h);
+      }
+    }
+  });
+}
+
 // ---- MLA absorbed decode ---------------------------------------------------------------
 // [ROCm-attn] "AITER MLA backend": DeepSeek-style MLA keeps one compressed 576-dim latent per
 // token in the KV cache; decode works directly in that latent space ("absorbed"): every query

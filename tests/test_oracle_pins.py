@@ -541,6 +541,55 @@ def test_fp8_decode_matches_torch_sdpa_on_dequantised_cache():
         assert np.abs(lse[r] - lse_ref(qf[r:r + 1], k, scale)[0]).max() < TOL
 
 
+def test_fp8_extend_matches_torch_sdpa_on_dequantised_context():
+    """Extend over an E4M3 cache == fp64 SDPA (causal over the new tokens) with the cached keys
+    and values dequantised (codes through torch's float8 decoding, times the scales) and the
+    new tokens' bf16 rows as given."""
+    b = _extend_case()
+    rng = np.random.default_rng(36)
+    kc = rng.integers(0, 256, size=tuple(b.k_cache.shape), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=tuple(b.v_cache.shape), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x31                                      # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x42
+    ks, vs, scale = 0.015, 0.3, 1 / math.sqrt(b.D)
+    out, lse = oracle.extend_fp8(gen.bf16_bits(b.q), gen.bf16_bits(b.k_new), gen.bf16_bits(b.v_new),
+                                 b.cu_q.numpy(), b.seq_lens.numpy(), kc, vc, b.block_tables.numpy(), scale, ks, vs)
+    deq = lambda c, s: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64) * s
+    kd, vd = deq(kc, ks).numpy(), deq(vc, vs).numpy()
+    qf, kf, vf = (f64(gen.bf16_bits(t)) for t in (b.q, b.k_new, b.v_new))
+    cu = b.cu_q.numpy()
+    for r in range(b.R):
+        s, e = cu[r], cu[r + 1]
+        C = b.seq_lens_list[r] - b.q_lens[r]
+        pos = np.arange(C)
+        blk = b.block_tables.numpy()[r, pos // 16]
+        k = torch.cat([torch.from_numpy(kd[blk, pos % 16]), kf[s:e]])
+        v = torch.cat([torch.from_numpy(vd[blk, pos % 16]), vf[s:e]])
+        exp = sdpa(qf[s:e], k, v, scale, causal_offset=C)
+        assert np.abs(out[s:e] - exp).max() < TOL
+        assert np.abs(lse[s:e] - lse_ref(qf[s:e], k, scale, C)).max() < TOL
+
+
+def test_fp8_extend_with_power_of_two_scales_is_the_bf16_extend():
+    """With scales that are powers of two the dequantised values are exact bf16 numbers: the
+    FP8 extend then equals the bf16 extend over a cache holding those numbers."""
+    b = _extend_case()
+    rng = np.random.default_rng(37)
+    kc = rng.integers(0, 256, size=tuple(b.k_cache.shape), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=tuple(b.v_cache.shape), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x25
+    vc[(vc & 0x7F) == 0x7F] = 0x26
+    ks, vs, scale = 2.0 ** -4, 2.0 ** -1, 0.2
+    out, lse = oracle.extend_fp8(gen.bf16_bits(b.q), gen.bf16_bits(b.k_new), gen.bf16_bits(b.v_new),
+                                 b.cu_q.numpy(), b.seq_lens.numpy(), kc, vc, b.block_tables.numpy(), scale, ks, vs)
+    to_bf16 = lambda c, s: gen.bf16_bits((torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float32) * s)
+                                         .to(torch.bfloat16))
+    ref, ref_lse = oracle.extend(gen.bf16_bits(b.q), gen.bf16_bits(b.k_new), gen.bf16_bits(b.v_new), b.cu_q.numpy(),
+                                 scale, seq_lens=b.seq_lens.numpy(), k_cache=to_bf16(kc, ks), v_cache=to_bf16(vc, vs),
+                                 block_tables=b.block_tables.numpy())
+    assert np.abs(out - ref).max() < 1e-12 and np.abs(lse - ref_lse).max() < 1e-12
+
+
 # ---- MLA absorbed decode ----------------------------------------------------------------------------
 
 def test_mla_decode_matches_torch_sdpa_with_latent_values():

@@ -36,8 +36,9 @@
  *   "rocm-attention-backend" (MLA section) reads such a cache with a dequantising gather
  *   ("gather_and_maybe_dequant_cache"); its served models are FP8. kv_cache_write stores
  *   E4M3(float(x) * (1.0f / scale)), rounded to the nearest code (ties to even) and saturated
- *   at +-448; pack/unpack copy codes; paged_decode_attn dequantises as it reads (head_dim 128).
- *   extend_attn does not take an FP8 cache (PKV_ERR_UNSUPPORTED).
+ *   at +-448; pack/unpack copy codes; paged_decode_attn dequantises as it reads (head_dim 128);
+ *   extend_attn gathers the set's context into a bf16 pool of the E4M3 values first (see
+ *   pkv_extend_fp8_workspace_size).
  *
  * The batch (arrival order, the layout vLLM's model runner gives its attention backend)
  *   R requests; cu_q int32 [R+1]: request r owns query rows cu_q[r] .. cu_q[r+1]-1 of the
@@ -261,10 +262,18 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
  * host bounds on q_len and seq_len over the set.
  * chunk_budget_tokens: the context chunk budget (0 = whole context as one chunk); results do
  * not depend on it. The partials of the chunks are merged by LSE inside the kernel.
- * workspace: may be NULL (this version needs none); workspace_bytes is ignored then.
+ * workspace: for a bf16 cache it may be NULL (none is needed; pkv_extend_workspace_size
+ * returns 0). For an FP8 (E4M3) cache it must hold at least pkv_extend_fp8_workspace_size(
+ * reqs.max_reqs, reqs.batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim) bytes
+ * (else PKV_ERR_WORKSPACE): the context of the set's requests is gathered there as bf16
+ * (the MLA section's "gather and maybe dequant" of the cached context), exactly the E4M3
+ * values, and the scales are applied in the attention (keys with the softmax scale, values on
+ * the softmax weights); head_dim 64 or 128. The workspace is rewritten by every such call.
  * ------------------------------------------------------------------------------------- */
 size_t pkv_extend_workspace_size(int32_t max_reqs, int32_t max_q_len, int32_t num_q_heads,
                                  int32_t head_dim, int32_t chunk_budget_tokens);
+size_t pkv_extend_fp8_workspace_size(int32_t max_reqs, int32_t batch_reqs, int32_t max_seq_len,
+                                     int32_t max_blocks, int32_t num_kv_heads, int32_t head_dim);
 pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, int64_t num_tokens,
                            const int32_t* cu_q, const int32_t* seq_lens, pkv_cache cache,
                            const int32_t* block_tables, int32_t max_blocks, pkv_reqs reqs,

@@ -76,7 +76,7 @@ def _load():
                                           i32, i32, f64, P, P, P, i32]
             lib.oracle_extend.restype = None
             lib.oracle_extend_fp8.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, P, i32, i32, i32, i32,
-                                              f64, f64, f64, P, P, i32]
+                                              f64, f64, f64, P, P, P, i32]
             lib.oracle_extend_fp8.restype = None
             lib.oracle_extend_chunked.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, i32,
                                                   i32, i32, i32, f64, i64, P, P]
@@ -321,7 +321,7 @@ def prefill(q, k, v, cu_seqlens, scale, req_ids=None, n_req=None, row_mask=None,
 
 
 def extend_fp8(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, scale, k_scale, v_scale,
-               req_ids=None, n_req=None, nthreads=None, out=None, lse=None):
+               req_ids=None, n_req=None, row_mask=None, nthreads=None, out=None, lse=None):
     """Extend over an FP8 cache: k_cache / v_cache uint8 E4M3 codes [nb, bs, Hkv, D] standing for
     e4m3(code) * k_scale / v_scale; new tokens bf16 bits. Returns (out, lse) float64."""
     lib = _load()
@@ -333,6 +333,8 @@ def extend_fp8(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, 
     hkv = k_new.shape[1]
     if n_req is None:
         n_req = req_ids.shape[0] if req_ids is not None else cu_q.shape[0] - 1
+    if row_mask is not None:
+        row_mask = _c(row_mask, np.uint8)
     if out is None:
         out = np.full((T, Hq, D), np.nan)
     if lse is None:
@@ -340,7 +342,7 @@ def extend_fp8(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, 
     lib.oracle_extend_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(seq_lens), _ptr(k_cache),
                           _ptr(v_cache), k_cache.shape[0], k_cache.shape[1], _ptr(block_tables),
                           block_tables.shape[1], _ptr(req_ids), n_req, Hq, hkv, D, float(scale), float(k_scale),
-                          float(v_scale), _ptr(out), _ptr(lse), nthreads or default_threads())
+                          float(v_scale), _ptr(row_mask), _ptr(out), _ptr(lse), nthreads or default_threads())
     return out, lse
 
 

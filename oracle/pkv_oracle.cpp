@@ -573,7 +573,7 @@ void oracle_extend_fp8(const uint16_t* q, const uint16_t* k_new, const uint16_t*
                        const uint8_t* v_cache, int64_t num_blocks, int32_t bs,
                        const int32_t* block_tables, int32_t max_blocks, const int32_t* req_ids,
                        int32_t n_req, int32_t Hq, int32_t Hkv, int32_t D, double scale, double k_scale,
-                       double v_scale, double* out, double* lse, int32_t nthreads) {
+                       double v_scale, const uint8_t* row_mask, double* out, double* lse, int32_t nthreads) {
   const Paged P{nullptr, nullptr, num_blocks, bs, Hkv, D, block_tables, max_blocks};
   const int G = Hq / Hkv;
   parallel_for(static_cast<int64_t>(n_req) * Hkv, nthreads, [&](int64_t item) {
@@ -581,6 +581,9 @@ void oracle_extend_fp8(const uint16_t* q, const uint16_t* k_new, const uint16_t*
     const int kh = static_cast<int>(item % Hkv);
     const int64_t row0 = cu_q[r], nq = cu_q[r + 1] - cu_q[r];
     const int64_t C = std::max<int64_t>(0, seq_lens[r] - nq);
+    bool any = false;
+    for (int64_t i = 0; i < nq; ++i) any = any || !row_mask || row_mask[row0 + i];
+    if (!any) return;
     const int64_t nk = C + nq;
     std::vector<double> K(static_cast<size_t>(nk) * D), V(static_cast<size_t>(nk) * D), qd(D);
     for (int64_t j = 0; j < C; ++j) {
@@ -597,6 +600,7 @@ void oracle_extend_fp8(const uint16_t* q, const uint16_t* k_new, const uint16_t*
       }
     for (int64_t i = 0; i < nq; ++i) {
       const int64_t row = row0 + i;
+      if (row_mask && !row_mask[row]) continue;
       for (int g = 0; g < G; ++g) {
         const int h = kh * G + g;
         for (int d = 0; d < D; ++d) qd[d] = bf16_value(q[(row * Hq + h) * D + d]);

@@ -42,6 +42,7 @@ SIGNATURES = [
     ("pkv_paged_decode_attn", i32, [P, PkvCache, P, i32, P, P, PkvReqs, i32, i32, f32, P, P, P, sz, P]),
     ("pkv_paged_decode_attn_noalloc", i32, [P, PkvCache, P, i32, P, P, PkvReqs, i32, i32, f32, P, P, P]),
     ("pkv_mla_decode_workspace_size", sz, [i32, i32, i32]),
+    ("pkv_extend_fp8_workspace_size", sz, [i32, i32, i32, i32, i32, i32]),
     ("pkv_mla_decode_attn", i32, [P, PkvCache, P, i32, P, P, PkvReqs, i32, i32, f32, i32, P, P, P, sz, P]),
     ("pkv_extend_workspace_size", sz, [i32, i32, i32, i32, i32]),
     ("pkv_extend_attn", i32, [P, P, P, i64, P, P, PkvCache, P, i32, PkvReqs, i32, i32, i32, i32, f32,

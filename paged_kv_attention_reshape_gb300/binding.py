@@ -239,15 +239,17 @@ def mla_decode_workspace_size(max_reqs, num_q_heads, max_seq_len) -> int:
 
 def extend_attn(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables, max_q_len,
                 max_seq_len, reqs: Optional[Reqs] = None, chunk_budget_tokens=32768, scale=None,
-                out=None, lse=None, stream=None):
-    """New tokens attend to their cached context (paged) and causally to themselves."""
+                out=None, lse=None, stream=None, k_scale=1.0, v_scale=1.0, workspace=None):
+    """New tokens attend to their cached context (paged) and causally to themselves. An FP8
+    cache (uint8 / float8 codes with per-tensor scales) is gathered into a bf16 workspace of
+    the set's context first (allocated here when not given)."""
     lib = _lib.load()
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
         _need(t, torch.bfloat16, n)
     _need(cu_q, torch.int32, "cu_q")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(block_tables, torch.int32, "block_tables")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     T, Hq, D = q.shape
     R = seq_lens.numel()
     reqs = reqs or Reqs(max_reqs=R, batch_reqs=R)
@@ -255,11 +257,22 @@ def extend_attn(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    need = 0
+    if cache.kv_dtype == _lib.KV_FP8_E4M3:
+        need = extend_fp8_workspace_size(reqs.max_reqs, reqs.batch_reqs, max_seq_len, block_tables.shape[1],
+                                         cache.num_kv_heads, cache.head_dim)
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(lib.pkv_extend_attn(_ptr(q), _ptr(k_new), _ptr(v_new), T, _ptr(cu_q), _ptr(seq_lens), cache,
                                _ptr(block_tables), block_tables.shape[1], reqs.c(), Hq, max_q_len,
                                max_seq_len, chunk_budget_tokens, _scale(scale, D), _ptr(out),
-                               _ptr(lse), None, 0, _stream(stream)), "extend_attn")
+                               _ptr(lse), _ptr(workspace) if need else None, need, _stream(stream)), "extend_attn")
     return out, lse
+
+
+def extend_fp8_workspace_size(max_reqs, batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim) -> int:
+    return int(_lib.load().pkv_extend_fp8_workspace_size(max_reqs, batch_reqs, max_seq_len, max_blocks,
+                                                         num_kv_heads, head_dim))
 
 
 def varlen_prefill_attn(q, k, v, cu_seqlens, max_seqlen, reqs: Optional[Reqs] = None, scale=None,

@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -453,12 +454,15 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
 size_t pkv_extend_workspace_size(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 // Extend (cache != NULL) and prefill (cache == NULL) share the checks and the kernel.
+// ctx_k_scale / ctx_v_scale: scales of the cached context's keys and values (1 for a bf16
+// cache; an FP8 context arrives here as a bf16 pool of the E4M3 values themselves).
 static pkv_status run_attention(const void* q, const void* k, const void* v, int64_t num_tokens,
                                 const int32_t* cu_q, const int32_t* seq_lens,
                                 const pkv_cache* cache, const int32_t* block_tables,
                                 int32_t max_blocks, pkv_reqs reqs, int32_t Hq, int32_t Hkv,
                                 int32_t D, int32_t max_q_len, int32_t max_seq_len, float scale,
-                                void* out, float* lse, pkv_stream_t stream) {
+                                void* out, float* lse, pkv_stream_t stream, float ctx_k_scale = 1.f,
+                                float ctx_v_scale = 1.f) {
   pkv_status st = check_reqs(reqs);
   if (st != PKV_OK) return st;
   if (cache != nullptr && (st = check_cache(*cache, true)) != PKV_OK) return st;
@@ -496,6 +500,8 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   p.max_q_len = max_q_len;
   p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.ctx_scale_log2 = scale * ctx_k_scale * 1.4426950408889634f;
+  p.ctx_v_scale = ctx_v_scale;
   CUtensorMap tq, tk, tv, tck, tcv;
   std::memset(&tck, 0, sizeof tck);
   std::memset(&tcv, 0, sizeof tcv);
@@ -512,18 +518,101 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   return st;
 }
 
+namespace {
+// The FP8 extend's workspace: the bf16 pools of K and V ([pool_blocks][16][Hkv][D] each), then
+// the pool's block table [batch_reqs][max_blocks]; each part 256-byte aligned.
+struct Fp8ExtendLayout {
+  int64_t pool_blocks;
+  size_t k_off, v_off, table_off, bytes;
+};
+Fp8ExtendLayout fp8_extend_layout(int32_t max_reqs, int32_t batch_reqs, int32_t max_seq_len, int32_t max_blocks,
+                                  int32_t Hkv, int32_t D) {
+  Fp8ExtendLayout L{};
+  const int64_t per_req = std::min<int64_t>((static_cast<int64_t>(max_seq_len) + 15) / 16, max_blocks);
+  L.pool_blocks = static_cast<int64_t>(max_reqs) * std::max<int64_t>(per_req, 0);
+  const size_t pool_bytes = static_cast<size_t>(L.pool_blocks) * 16 * Hkv * D * 2;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  L.k_off = 0;
+  L.v_off = up(pool_bytes);
+  L.table_off = L.v_off + up(pool_bytes);
+  L.bytes = L.table_off + up(static_cast<size_t>(batch_reqs) * std::max(max_blocks, 0) * 4);
+  return L;
+}
+}  // namespace
+
+size_t pkv_extend_fp8_workspace_size(int32_t max_reqs, int32_t batch_reqs, int32_t max_seq_len,
+                                     int32_t max_blocks, int32_t num_kv_heads, int32_t head_dim) {
+  if (max_reqs < 0 || batch_reqs < 0 || max_seq_len < 0 || max_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return 0;
+  return fp8_extend_layout(max_reqs, batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim).bytes;
+}
+
 pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, int64_t num_tokens,
                            const int32_t* cu_q, const int32_t* seq_lens, pkv_cache cache,
                            const int32_t* block_tables, int32_t max_blocks, pkv_reqs reqs,
                            int32_t num_q_heads, int32_t max_q_len, int32_t max_seq_len,
                            int32_t chunk_budget_tokens, float scale, void* out, float* lse,
                            void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (chunk_budget_tokens < 0) return PKV_ERR_INVALID_ARG;
-  return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &cache, block_tables,
-                       max_blocks, reqs, num_q_heads, cache.num_kv_heads, cache.head_dim,
-                       max_q_len, max_seq_len, scale, out, lse, stream);
+  if (cache.kv_dtype != PKV_KV_FP8_E4M3)
+    return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &cache, block_tables,
+                         max_blocks, reqs, num_q_heads, cache.num_kv_heads, cache.head_dim,
+                         max_q_len, max_seq_len, scale, out, lse, stream);
+  // FP8 cache: gather the set's context into a bf16 pool of the E4M3 values, then the bf16
+  // kernel over that pool with the scales applied per context tile
+  pkv_status st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if ((st = check_reqs(reqs)) != PKV_OK) return st;
+  const int Hkv = cache.num_kv_heads, D = cache.head_dim;
+  if ((D != 64 && D != 128) || cache.block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (!group_ok(num_q_heads, Hkv)) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
+  if (seq_lens == nullptr || block_tables == nullptr || max_blocks <= 0 || cu_q == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (reqs.max_reqs > 1024) return PKV_ERR_UNSUPPORTED;
+  const Fp8ExtendLayout L = fp8_extend_layout(reqs.max_reqs, reqs.batch_reqs, max_seq_len, max_blocks, Hkv, D);
+  if (workspace == nullptr || workspace_bytes < L.bytes || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  CtxDequantParams g{};
+  g.err = error_word();
+  g.order = reqs.order;
+  g.bounds = reqs.bounds;
+  g.cls = reqs.cls;
+  g.max_reqs = reqs.max_reqs;
+  g.batch_reqs = reqs.batch_reqs;
+  g.cu_q = cu_q;
+  g.seq_lens = seq_lens;
+  g.block_tables = block_tables;
+  g.max_blocks = max_blocks;
+  g.k_codes = static_cast<const uint8_t*>(cache.k);
+  g.v_codes = static_cast<const uint8_t*>(cache.v);
+  g.stride_block = cache.stride_block;
+  g.num_blocks = cache.num_blocks;
+  g.Hkv = Hkv;
+  g.D = D;
+  g.k_pool = reinterpret_cast<__nv_bfloat16*>(ws + L.k_off);
+  g.v_pool = reinterpret_cast<__nv_bfloat16*>(ws + L.v_off);
+  g.table_out = reinterpret_cast<int32_t*>(ws + L.table_off);
+  g.pool_blocks = L.pool_blocks;
+  if (L.pool_blocks > 0) {
+    st = cuda_status(launch_ctx_dequant(g, reinterpret_cast<cudaStream_t>(stream)));
+    t_launches += 1;
+    if (st != PKV_OK) return st;
+  }
+  pkv_cache pool{};
+  pool.k = g.k_pool;
+  pool.v = g.v_pool;
+  pool.num_blocks = L.pool_blocks > 0 ? L.pool_blocks : 1;
+  pool.block_size = 16;
+  pool.num_kv_heads = Hkv;
+  pool.head_dim = D;
+  pool.stride_block = static_cast<int64_t>(16) * Hkv * D;
+  pool.kv_dtype = PKV_KV_BF16;
+  pool.k_scale = pool.v_scale = 1.f;
+  return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &pool, g.table_out, max_blocks, reqs,
+                       num_q_heads, Hkv, D, max_q_len, max_seq_len, scale, out, lse, stream, cache.k_scale,
+                       cache.v_scale);
 }
 
 pkv_status pkv_varlen_prefill_attn(const void* q, const void* k, const void* v, int64_t num_tokens,

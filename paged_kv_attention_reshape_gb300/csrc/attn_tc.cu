@@ -28,6 +28,8 @@
 // then it keeps the stale max, and p <= 2^8 stays exact enough in bf16 and fp32.
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 #include "softmax.cuh"
@@ -144,7 +146,9 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, vol
   return __all_sync(0xffffffffu, tc_wait(bar, parity, abort_flag, err));
 }
 
-template <int D>
+// SCALED: the cached context holds the E4M3 values of an FP8 cache (gathered into bf16), whose
+// key and value scales apply per context tile; the bf16 cache's kernel has none of that code.
+template <int D, bool SCALED>
 __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
     const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -283,6 +287,11 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         else kv = min(128, qi - (j - it.nct) * 128 + 1);
         const bool full = __all_sync(0xffffffffu, kv >= 128);
         const uint32_t srow = tmem + lane_off + scol(slot);
+        // a context tile of an FP8 cache holds the E4M3 values themselves: its key scale goes
+        // with the softmax scale, its value scale onto P (the row sum stays unscaled)
+        const bool ctx = j < it.nct;
+        const float sl = SCALED && ctx ? p.ctx_scale_log2 : p.scale_log2;
+        const bool vsc = SCALED && ctx && p.ctx_v_scale != 1.f;
         // pass 1: row max of the raw scores (the scale is positive, so it commutes with max)
         float mx = -CUDART_INF_F;
 #pragma unroll
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
               if (c * 32 + e < kv) mx = fmaxf(mx, __uint_as_float(v[e]));
           }
         }
-        mx = mx * p.scale_log2;  // -inf stays -inf
+        mx = mx * sl;  // -inf stays -inf
         float alpha = 1.f;
         if (mx > m + 8.f || m == -CUDART_INF_F) {  // lazy rescale: only when the max really grows
           const float m_new = fmaxf(m, mx);
@@ -311,10 +320,11 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         // pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs over the first half of S
         const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
         float rs = 0.f;
-        if (full) {
-          // every column valid: pairs of columns in packed fp32 (one instruction per pair for
-          // the scale-and-shift and the running sum)
-          const uint64_t sc2 = sm::f2(p.scale_log2, p.scale_log2), nm2 = sm::f2(neg_m, neg_m);
+        // every column valid: pairs of columns in packed fp32 (one instruction per pair for the
+        // scale-and-shift and the running sum); with a value scale, P is scaled as it is packed
+        auto full_pass = [&](auto scaled) {  // std::true_type: P scaled by the value scale
+          const uint64_t sc2 = sm::f2(sl, sl), nm2 = sm::f2(neg_m, neg_m);
+          const uint64_t vs2 = sm::f2(p.ctx_v_scale, p.ctx_v_scale);
           uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -329,13 +339,18 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
               sm::unf2(x, x0, x1);
               const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
               rs2 = sm::add2(rs2, pp);
-              pk[e / 2] = sm::bf16x2(pp);
+              if constexpr (decltype(scaled)::value) pk[e / 2] = sm::bf16x2(sm::mul2(pp, vs2));
+              else pk[e / 2] = sm::bf16x2(pp);
             }
             tc::st16(srow + c * 16, pk);
           }
           float r0, r1;
           sm::unf2(rs2, r0, r1);
-          rs = r0 + r1;
+          return r0 + r1;
+        };
+        if (full) {
+          if constexpr (SCALED) rs = vsc ? full_pass(std::true_type{}) : full_pass(std::false_type{});
+          else rs = full_pass(std::false_type{});
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -345,12 +360,13 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2, neg_m));
-              float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, neg_m));
+              float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl, neg_m));
+              float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl, neg_m));
               p0 = (c * 32 + e < kv) ? p0 : 0.f;
               p1 = (c * 32 + e + 1 < kv) ? p1 : 0.f;
               rs += p0 + p1;
-              pk[e / 2] = pack_bf16(p0, p1);
+              if constexpr (SCALED) pk[e / 2] = vsc ? pack_bf16(p0 * p.ctx_v_scale, p1 * p.ctx_v_scale) : pack_bf16(p0, p1);
+              else pk[e / 2] = pack_bf16(p0, p1);
             }
             tc::st16(srow + c * 16, pk);
           }
@@ -567,16 +583,16 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
   }
 }
 
-template <int D>
+template <int D, bool SCALED>
 static cudaError_t launch_attention_tc_impl(const AttnParams& p, const CUtensorMap& tq,
                                             const CUtensorMap& tk, const CUtensorMap& tv,
                                             const CUtensorMap& tck, const CUtensorMap& tcv,
                                             cudaStream_t stream, int* launches) {
   using C = TcCfg<D>;
-  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&attention_tc_kernel<D>), C::SMEM,
-                                     D == 64 ? kAttrAttn64 : kAttrAttn128);
+  const int slot = SCALED ? (D == 64 ? kAttrAttn64Scaled : kAttrAttn128Scaled) : (D == 64 ? kAttrAttn64 : kAttrAttn128);
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&attention_tc_kernel<D, SCALED>), C::SMEM, slot);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attention_tc_kernel<D>, dim3(num_sms()), dim3(C::THREADS), C::SMEM, stream, p, tq, tk, tv,
+  e = launch_pdl(attention_tc_kernel<D, SCALED>, dim3(num_sms()), dim3(C::THREADS), C::SMEM, stream, p, tq, tk, tv,
                  tck, tcv);
   *launches += 1;
   return e;
@@ -585,8 +601,11 @@ static cudaError_t launch_attention_tc_impl(const AttnParams& p, const CUtensorM
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const CUtensorMap& tm_ck,
                              const CUtensorMap& tm_cv, int D, cudaStream_t stream, int* launches) {
-  return D == 64 ? launch_attention_tc_impl<64>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches)
-                 : launch_attention_tc_impl<128>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
+  const bool scaled = p.ctx_scale_log2 != p.scale_log2 || p.ctx_v_scale != 1.f;
+  if (scaled)
+    return D == 64 ? launch_attention_tc_impl<64, true>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches)
+                   : launch_attention_tc_impl<128, true>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
+  return D == 64 ? launch_attention_tc_impl<64, false>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches)
+                 : launch_attention_tc_impl<128, false>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
 }
-
 }  // namespace pkv

@@ -62,6 +62,30 @@ struct AttnParams {
   int32_t max_q_len;
   int32_t max_seq_len;
   float scale_log2;
+  float ctx_scale_log2;  // cached-context key tiles: softmax scale * key scale * log2(e)
+  float ctx_v_scale;     // cached-context tiles: P is multiplied by the value scale for P V
+};
+
+// Extend over an FP8 cache: the set's context blocks gathered into a bf16 pool (exact E4M3
+// values) with a block table of the pool.
+struct CtxDequantParams {
+  unsigned int* err;
+  const int32_t* order;
+  const int32_t* bounds;
+  int32_t cls, max_reqs, batch_reqs;
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  int64_t stride_block;  // bytes between consecutive cache blocks
+  int64_t num_blocks;
+  int32_t Hkv, D;
+  __nv_bfloat16* k_pool;
+  __nv_bfloat16* v_pool;
+  int32_t* table_out;    // [batch_reqs][max_blocks]
+  int64_t pool_blocks;
 };
 
 // Launch with programmatic stream serialisation: the kernel may begin launching while the
@@ -89,6 +113,8 @@ enum AttrSlot {
   kAttrDecode128Fp8,
   kAttrAttn64,
   kAttrAttn128,
+  kAttrAttn64Scaled,
+  kAttrAttn128Scaled,
   kAttrMla,
   kAttrCount
 };
@@ -115,6 +141,7 @@ cudaError_t launch_paged_decode(const DecodeParams& p, const CUtensorMap& tk, co
 int decode_smem_bytes(int D);
 size_t decode_workspace_bytes(int Hq, int Hkv, int D);
 size_t decode_workspace_ctr_offset(int Hq, int Hkv, int D);
+cudaError_t launch_ctx_dequant(const CtxDequantParams& p, cudaStream_t stream);
 // Absorbed MLA decode: tm over the latent cache (one 576-wide head, bf16).
 cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, int* launches);
 size_t mla_workspace_bytes(int Hq);

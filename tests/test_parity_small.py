@@ -247,12 +247,57 @@ def test_decode_fp8_peaked_softmax(pkv):
     compare_attention(out, lse, ref, ref_lse, what="decode fp8 peaked")
 
 
-def test_extend_rejects_fp8_cache(pkv):
-    b = gen.extend_batch([5], [20], Hq=8, Hkv=2, D=128, seed=62)
-    kc = torch.zeros(tuple(b.k_cache.shape), dtype=torch.uint8, device=DEV)
-    with pytest.raises(pkv.PkvError):
-        pkv.extend_attn(b.q.to(DEV), b.k_new.to(DEV), b.v_new.to(DEV), b.cu_q.to(DEV), b.seq_lens.to(DEV),
-                        kc, kc.clone(), b.block_tables.to(DEV), 5, 25)
+def _fp8_extend_ref(b, kc, vc, ks, vs, scale, **kw):
+    return oracle.extend_fp8(bits(b.q), bits(b.k_new), bits(b.v_new), b.cu_q.cpu().numpy(), b.seq_lens.cpu().numpy(),
+                             kc, vc, b.block_tables.cpu().numpy(), scale, ks, vs, **kw)
+
+
+@pytest.mark.parametrize("G,D", [(1, 64), (4, 128), (8, 128), (16, 64)])
+def test_extend_fp8_ragged(pkv, G, D):
+    """Extend over an E4M3 cache: the set's context gathered into a bf16 pool of the E4M3
+    values, the scales applied in the attention; ragged new and cached lengths."""
+    Hkv = 2
+    new = [1, 63, 64, 65, 130, 7]
+    ctx = [0, 1, 15, 16, 100, 300]
+    b = gen.extend_batch(new, ctx, Hq=G * Hkv, Hkv=Hkv, D=D, seed=G * 11 + D)
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kc.to(DEV), vc.to(DEV), g.block_tables,
+                               max(new), max(b.seq_lens_list), scale=scale, k_scale=ks, v_scale=vs)
+    ref, ref_lse = _fp8_extend_ref(b, kc.numpy(), vc.numpy(), ks, vs, scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"extend fp8 G={G} D={D}")
+    assert _errors(pkv) == 0
+
+
+def test_extend_fp8_request_set_and_peaked(pkv):
+    """A request set from the reorder's outputs over a shuffled batch, peaked queries, and
+    NaN codes past the end of each context (never gathered into a sum)."""
+    b = gen.mixed_batch(4, (20, 90), 5, 70, (10, 400), 3, (5, 80), Hq=16, Hkv=2, D=128, seed=63, q_scale=3.0)
+    ks, vs = gen.fp8_scale(6.0), gen.fp8_scale(5.0)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    bt = b.block_tables.numpy()
+    for r in range(b.R):
+        C = b.seq_lens_list[r] - b.q_lens[r]
+        if C % 16:
+            kc[bt[r, C // 16], C % 16:] = 0x7F
+            vc[bt[r, C // 16], C % 16:] = 0xFF
+    g = b.to(DEV)
+    R = b.R
+    perm, bounds, _, _ = pkv.batch_classify_reorder(g.cu_q, g.seq_lens)
+    reqs = pkv.Reqs(max_reqs=R, batch_reqs=R, order=perm, bounds=bounds, cls=pkv.CLASS_EXTEND)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((b.T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    scale = default_scale(128)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kc.to(DEV), vc.to(DEV), g.block_tables,
+                    max(b.q_lens), max(b.seq_lens_list), reqs=reqs, scale=scale, k_scale=ks, v_scale=vs,
+                    out=out, lse=lse)
+    o_perm, o_bounds, _, _ = oracle.batch_classify_reorder(b.cu_q.numpy(), b.seq_lens.numpy())
+    ids = o_perm[o_bounds[1]:o_bounds[2]]
+    ref, ref_lse = _fp8_extend_ref(b, kc.numpy(), vc.numpy(), ks, vs, scale, req_ids=ids)
+    compare_attention(out, lse, ref, ref_lse, what="extend fp8 set")
+    assert _errors(pkv) == 0
 
 
 # ---- failure detection -----------------------------------------------------------------------

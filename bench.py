@@ -545,6 +545,57 @@ def bench_mixed(pkv, dev, stream, timer, steps, warmup):
                 ext_flops=ext_flops, pre_flops=pre_flops)
 
 
+def bench_mixed_fp8(pkv, dev, stream, timer, steps, warmup):
+    """The mixed step over an FP8 (E4M3) cache: quantising write, decode dequantising as it
+    reads, extend through the gather of its context into a bf16 workspace, prefill (no cache)."""
+    b = mixed_workload(dev)
+    R, T = b.R, b.T
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    del b.k_cache, b.v_cache
+    torch.cuda.empty_cache()
+    meta = dict(cu_q=b.cu_q.to(dev), seq_lens=b.seq_lens.to(dev), block_tables=b.block_tables.to(dev),
+                slot_mapping=b.slot_mapping.to(dev))
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    bounds = torch.empty(4, dtype=torch.int32, device=dev)
+    out = torch.empty_like(b.q)
+    lse = torch.empty((T, b.Hq), dtype=torch.float32, device=dev)
+    kinds = b.kinds
+    n_dec = sum(k == gen.DECODE for k in kinds)
+    n_ext = sum(k == gen.EXTEND for k in kinds)
+    n_pre = sum(k == gen.PREFILL for k in kinds)
+    max_dec = max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.DECODE)
+    max_ext_q = max(q for k, q in zip(kinds, b.q_lens) if k == gen.EXTEND)
+    max_ext_s = max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.EXTEND)
+    max_pre = max(q for k, q in zip(kinds, b.q_lens) if k == gen.PREFILL)
+    ws = torch.empty(max(pkv.paged_decode_workspace_size(n_dec, b.Hq, b.Hkv, b.D, max_dec), 16), dtype=torch.uint8,
+                     device=dev)
+    ews = torch.empty(max(pkv.extend_fp8_workspace_size(n_ext, R, max_ext_s, b.block_tables.shape[1], b.Hkv, b.D), 16),
+                      dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(b.D)
+
+    def step(marks):
+        mark(marks, "reorder", stream, lambda: pkv.batch_classify_reorder(
+            meta["cu_q"], meta["seq_lens"], perm=perm, bounds=bounds, stream=stream))
+        mark(marks, "write", stream, lambda: pkv.kv_cache_write(
+            b.k_new, b.v_new, meta["slot_mapping"], kc, vc, stream=stream, k_scale=ks, v_scale=vs))
+        mark(marks, "decode", stream, lambda: pkv.paged_decode_attn(
+            b.q, kc, vc, meta["block_tables"], meta["seq_lens"], max_dec, cu_q=meta["cu_q"],
+            reqs=pkv.Reqs(n_dec, R, perm, bounds, pkv.CLASS_DECODE), scale=scale, out=out, lse=lse,
+            workspace=ws, stream=stream, k_scale=ks, v_scale=vs))
+        mark(marks, "extend", stream, lambda: pkv.extend_attn(
+            b.q, b.k_new, b.v_new, meta["cu_q"], meta["seq_lens"], kc, vc, meta["block_tables"], max_ext_q,
+            max_ext_s, reqs=pkv.Reqs(n_ext, R, perm, bounds, pkv.CLASS_EXTEND), scale=scale, out=out, lse=lse,
+            stream=stream, k_scale=ks, v_scale=vs, workspace=ews))
+        mark(marks, "prefill", stream, lambda: pkv.varlen_prefill_attn(
+            b.q, b.k_new, b.v_new, meta["cu_q"], max_pre, reqs=pkv.Reqs(n_pre, R, perm, bounds, pkv.CLASS_PREFILL),
+            scale=scale, out=out, lse=lse, stream=stream))
+
+    ms, sec = timer.run(step, steps, warmup)
+    errs = pkv.device_errors(clear=True)
+    return dict(ms=ms, sec=sec, tokens=T, errors=errs, ws_bytes=ews.numel())
+
+
 def bench_attention_only(pkv, dev, stream, timer, steps, warmup, kind):
     """Prefill 4 x 8192 or the long-context extend (2 x (100k cached + 2048 new))."""
     if kind == "prefill":
@@ -828,6 +879,19 @@ def main():
             del m
         except Exception as e:  # report, keep the headline
             extras["mixed_batch"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            m8 = bench_mixed_fp8(pkv, dev, stream, timer, steps, warmup)
+            mms8 = sum(m8["ms"]) / len(m8["ms"])
+            extras["mixed_batch_fp8"] = {
+                "workload": "the mixed batch over an FP8 (E4M3, per-tensor scale) cache: quantising write, "
+                            "decode dequantising as it reads, extend through the gather of its context into bf16",
+                "tokens_per_s": m8["tokens"] / (mms8 * 1e-3), "ms_per_step": mms8,
+                "per_call_ms": {k: sum(v) / len(v) for k, v in m8["sec"].items()},
+                "extend_workspace_bytes": m8["ws_bytes"], "device_errors": m8["errors"],
+            }
+        except Exception as e:
+            extras["mixed_batch_fp8"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             r = bench_decode_fp8(pkv, dev, stream, timer, steps, warmup)

@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxReqs = 1024;  // set positions handled (the extend kernel's limit)
+constexpr int kPer = 4;         // 16-byte chunks of K (and of V) a thread loads at once
 
 // Four E4M3 codes (one 32-bit word) as four bf16 values, exactly (every E4M3 number is a bf16
 // number): through fp16, which holds them exactly too.
@@ -93,9 +94,11 @@ __global__ void __launch_bounds__(kThreads) ctx_dequant_kernel(CtxDequantParams 
     total = p.pool_blocks;
   }
 
-  // one context block: 16 rows x Hkv x D codes of K and of V -> bf16 pool block g
+  // one context block: 16 rows x Hkv x D codes of K and of V -> bf16 pool block g, 16 codes
+  // (one 16-byte load) at a time; a thread's loads of the block are all issued before the
+  // first conversion
   const int64_t row_codes = static_cast<int64_t>(p.Hkv) * p.D;  // codes of one token row
-  const int words = static_cast<int>(16 * row_codes / 4);       // 32-bit words of a block
+  const int chunks = static_cast<int>(16 * row_codes / 16);      // 16-byte chunks of a block
   for (int g = blockIdx.x; g < total; g += gridDim.x) {
     int a = 0, z = n - 1;  // the set position whose range holds g
     while (a < z) {
@@ -110,14 +113,32 @@ __global__ void __launch_bounds__(kThreads) ctx_dequant_kernel(CtxDequantParams 
     if (!good && tid == 0) flag_error(p.err, PKV_DEVERR_BLOCK);
     if (tid == 0) p.table_out[static_cast<int64_t>(r) * p.max_blocks + j] = g;
     const int64_t src_off = static_cast<int64_t>(good ? src : 0) * p.stride_block;
-    const uint32_t* sk = reinterpret_cast<const uint32_t*>(p.k_codes + src_off);
-    const uint32_t* sv = reinterpret_cast<const uint32_t*>(p.v_codes + src_off);
-    uint2* dk = reinterpret_cast<uint2*>(p.k_pool + static_cast<int64_t>(g) * 16 * row_codes);
-    uint2* dv = reinterpret_cast<uint2*>(p.v_pool + static_cast<int64_t>(g) * 16 * row_codes);
-    for (int e = tid; e < words; e += kThreads) {
-      const uint32_t kw = good ? __ldg(sk + e) : 0u, vw = good ? __ldg(sv + e) : 0u;
-      dk[e] = e4m3x4_to_bf16x4(kw);
-      dv[e] = e4m3x4_to_bf16x4(vw);
+    const uint4* sk = reinterpret_cast<const uint4*>(p.k_codes + src_off);
+    const uint4* sv = reinterpret_cast<const uint4*>(p.v_codes + src_off);
+    uint4* dk = reinterpret_cast<uint4*>(p.k_pool + static_cast<int64_t>(g) * 16 * row_codes);
+    uint4* dv = reinterpret_cast<uint4*>(p.v_pool + static_cast<int64_t>(g) * 16 * row_codes);
+    for (int e0 = 0; e0 < chunks; e0 += kThreads * kPer) {
+      uint4 kq[kPer], vq[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = e0 + u * kThreads + tid;
+        const bool in = good && e < chunks;
+        kq[u] = in ? __ldg(sk + e) : make_uint4(0, 0, 0, 0);
+        vq[u] = in ? __ldg(sv + e) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = e0 + u * kThreads + tid;
+        if (e >= chunks) continue;
+        const uint2 k0 = e4m3x4_to_bf16x4(kq[u].x), k1 = e4m3x4_to_bf16x4(kq[u].y);
+        const uint2 k2 = e4m3x4_to_bf16x4(kq[u].z), k3 = e4m3x4_to_bf16x4(kq[u].w);
+        const uint2 v0 = e4m3x4_to_bf16x4(vq[u].x), v1 = e4m3x4_to_bf16x4(vq[u].y);
+        const uint2 v2 = e4m3x4_to_bf16x4(vq[u].z), v3 = e4m3x4_to_bf16x4(vq[u].w);
+        dk[2 * e] = make_uint4(k0.x, k0.y, k1.x, k1.y);
+        dk[2 * e + 1] = make_uint4(k2.x, k2.y, k3.x, k3.y);
+        dv[2 * e] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+        dv[2 * e + 1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+      }
     }
   }
 }

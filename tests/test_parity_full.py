@@ -153,6 +153,59 @@ def test_mixed_llama70b_full(pkv):
     print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="mixed llama70b full"))
 
 
+def test_mixed_llama70b_fp8_full(pkv):
+    """The mixed step over an FP8 (E4M3) cache: quantising write, decode dequantising as it
+    reads, extend through the gather of its context into bf16; the written caches bit for bit,
+    sampled decode and extend rows against the FP8 oracles."""
+    b = gen.mixed_batch(**gen.MIXED_LLAMA70B, device="cuda")
+    ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+    kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+    del b.k_cache, b.v_cache
+    kc0, vc0 = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+    R, T = b.R, b.T
+    kinds = b.kinds
+    n_dec = sum(k == gen.DECODE for k in kinds)
+    n_ext = sum(k == gen.EXTEND for k in kinds)
+    perm, bounds, _, _ = pkv.batch_classify_reorder(b.cu_q, b.seq_lens)
+    pkv.kv_cache_write(b.k_new, b.v_new, b.slot_mapping, kc, vc, k_scale=ks, v_scale=vs)
+    out = torch.full_like(b.q, float("nan"))
+    lse = torch.full((T, b.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    scale = 1 / math.sqrt(b.D)
+    pkv.paged_decode_attn(b.q, kc, vc, b.block_tables, b.seq_lens,
+                          max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.DECODE), cu_q=b.cu_q,
+                          reqs=pkv.Reqs(n_dec, R, perm, bounds, pkv.CLASS_DECODE), scale=scale, out=out, lse=lse,
+                          k_scale=ks, v_scale=vs)
+    pkv.extend_attn(b.q, b.k_new, b.v_new, b.cu_q, b.seq_lens, kc, vc, b.block_tables,
+                    max(q for k, q in zip(kinds, b.q_lens) if k == gen.EXTEND),
+                    max(s for k, s in zip(kinds, b.seq_lens_list) if k == gen.EXTEND),
+                    reqs=pkv.Reqs(n_ext, R, perm, bounds, pkv.CLASS_EXTEND), scale=scale, out=out, lse=lse,
+                    k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkv.device_errors() == 0
+    assert oracle.kv_cache_write_fp8(_host(b.k_new), _host(b.v_new), b.slot_mapping.cpu().numpy(), kc0, vc0,
+                                     ks, vs) == 0
+    assert np.array_equal(kc.cpu().numpy(), kc0) and np.array_equal(vc.cpu().numpy(), vc0)
+    e_perm, e_bounds, _, _ = oracle.batch_classify_reorder(b.cu_q.cpu().numpy(), b.seq_lens.cpu().numpy())
+    rng = np.random.default_rng(2)
+    cu = b.cu_q.cpu().numpy()
+    d_sample = np.sort(rng.choice(e_perm[:n_dec], 16, replace=False)).astype(np.int32)
+    rows = np.zeros(T, bool)
+    for r in d_sample:
+        rows[cu[r]] = True
+    for r in e_perm[n_dec:n_dec + n_ext]:
+        n = cu[r + 1] - cu[r]
+        for i in {0, n - 1, *rng.choice(n, 4, replace=False).tolist()}:
+            rows[cu[r] + i] = True
+    ref = np.full((T, b.Hq, b.D), np.nan)
+    ref_lse = np.full((T, b.Hq), np.nan)
+    qb, kb, vb = _host(b.q), _host(b.k_new), _host(b.v_new)
+    bt, sl = b.block_tables.cpu().numpy(), b.seq_lens.cpu().numpy()
+    oracle.paged_decode_fp8(qb, kc0, vc0, bt, sl, scale, ks, vs, cu_q=cu, req_ids=d_sample, out=ref, lse=ref_lse)
+    oracle.extend_fp8(qb, kb, vb, cu, sl, kc0, vc0, bt, scale, ks, vs, req_ids=e_perm[n_dec:n_dec + n_ext],
+                      row_mask=rows, out=ref, lse=ref_lse)
+    print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="mixed llama70b fp8 full"))
+
+
 def test_long_extend_full(pkv):
     """2 x (100000 cached + 2048 new), budget 32768: 24 sampled rows (first/last of each request)."""
     b = gen.extend_batch(**gen.LONG_EXTEND, device="cuda")

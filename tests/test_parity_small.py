@@ -300,6 +300,66 @@ def test_extend_fp8_request_set_and_peaked(pkv):
     assert _errors(pkv) == 0
 
 
+# ---- randomized shapes -------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_mixed_batches(pkv, seed):
+    """Random mixes of decode, extend and prefill requests (lengths from 1 token to several
+    tiles, random head counts and head dims, shuffled arrival order) through the whole step:
+    reorder, write, then the three attention calls on the reorder's sets; every row checked."""
+    rng = np.random.default_rng(1000 + seed)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    n_dec, n_ext, n_pre = (int(x) for x in rng.integers(0, 6, size=3))
+    if n_dec + n_ext + n_pre == 0:
+        n_dec = 1
+    b = gen.mixed_batch(n_dec, (1, int(rng.integers(2, 900))), n_ext, int(rng.integers(1, 300)),
+                        (1, int(rng.integers(2, 700))), n_pre, (1, int(rng.integers(2, 400))),
+                        Hq=G * Hkv, Hkv=Hkv, D=D, seed=2000 + seed)
+    g = b.to(DEV)
+    R, T = b.R, b.T
+    perm, bounds, _, _ = pkv.batch_classify_reorder(g.cu_q, g.seq_lens)
+    pkv.kv_cache_write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    scale = default_scale(D)
+    maxs, maxq = max(b.seq_lens_list), max(b.q_lens)
+    mk = lambda c: pkv.Reqs(max_reqs=R, batch_reqs=R, order=perm, bounds=bounds, cls=c)
+    pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, maxs, cu_q=g.cu_q,
+                          reqs=mk(pkv.CLASS_DECODE), scale=scale, out=out, lse=lse)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, g.k_cache, g.v_cache, g.block_tables, maxq, maxs,
+                    reqs=mk(pkv.CLASS_EXTEND), scale=scale, out=out, lse=lse)
+    pkv.varlen_prefill_attn(g.q, g.k_new, g.v_new, g.cu_q, maxq, reqs=mk(pkv.CLASS_PREFILL), scale=scale,
+                            out=out, lse=lse)
+    assert _errors(pkv) == 0
+    kc, vc = bits(b.k_cache).copy(), bits(b.v_cache).copy()
+    assert oracle.kv_cache_write(bits(b.k_new), bits(b.v_new), b.slot_mapping.numpy(), kc, vc) == 0
+    o_perm, o_bounds, _, _ = oracle.batch_classify_reorder(b.cu_q.numpy(), b.seq_lens.numpy())
+    assert np.array_equal(perm.cpu().numpy(), o_perm) and np.array_equal(bounds.cpu().numpy(), o_bounds)
+    ref = np.full((T, b.Hq, D), np.nan)
+    ref_lse = np.full((T, b.Hq), np.nan)
+    qb = bits(b.q)
+    oracle.paged_decode(qb, kc, vc, b.block_tables.numpy(), b.seq_lens.numpy(), scale, cu_q=b.cu_q.numpy(),
+                        req_ids=o_perm[o_bounds[0]:o_bounds[1]], out=ref, lse=ref_lse)
+    oracle_extend(b, kc, vc, scale, req_ids=o_perm[o_bounds[1]:o_bounds[2]], out=ref, lse=ref_lse)
+    oracle_prefill(b, scale, req_ids=o_perm[o_bounds[2]:o_bounds[3]], out=ref, lse=ref_lse)
+    compare_attention(out, lse, ref, ref_lse, what=f"random mix {seed}: D={D} Hkv={Hkv} G={G}")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_mla_batches(pkv, seed):
+    rng = np.random.default_rng(3000 + seed)
+    Hq = int(rng.choice([16, 32, 64]))
+    R = int(rng.integers(1, 40))
+    lens = [int(x) for x in rng.integers(0, int(rng.choice([50, 2000, 20000])), size=R)]
+    b = gen.mla_batch(R, 0, 0, Hq=Hq, seq_lens=lens, seed=4000 + seed)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what=f"random mla {seed}: Hq={Hq} R={R}")
+    assert _errors(pkv) == 0
+
+
 # ---- failure detection -----------------------------------------------------------------------
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable(pkv):

@@ -10,9 +10,11 @@
 //   * the work is the list of 16-token KV blocks of the set's sequences; a fixed grid of CTAs
 //     takes equal, contiguous shares of that list (a share may start or end inside a
 //     sequence), so every CTA streams the same number of bytes and no wave tail is left;
-//   * the warps of a CTA are the KV heads of a head group: warp w walks the CTA's share for KV
-//     head kh = group * warps + w. All warps of a CTA read the same physical blocks at about
-//     the same time, each its head's slice, so every 16 KB block is fetched as a whole;
+//   * a CTA runs a few consecutive shares side by side (about 8 warps per SM for a bf16 cache,
+//     12 for FP8, in one CTA where shared memory allows, so the set's tables are held once
+//     per SM); the warps of one share are the KV heads of a head group: warp w of the share
+//     walks it for KV head kh = group * hw + w. The warps of a share read the same physical
+//     blocks at about the same time, each its head's slice, so every block is fetched whole;
 //   * a warp streams its blocks itself: lane 0 issues TMA loads (128-byte swizzle, one box per
 //     64-wide half of head_dim and K/V) into the warp's own ring of NSW stages, NSW blocks
 //     ahead of the math; block-table entries come 32 at a time in one coalesced load, one
@@ -41,12 +43,12 @@ namespace pkv {
 
 // FP8: the cache holds E4M3 codes (one byte per element). A block row of one head is then
 // D bytes (one 128-byte TMA box at D = 128) and a stage half as large; the smaller rings let
-// three CTAs share an SM (12 warps instead of 8, at most 168 registers each), which the
-// conversions of the codes need to keep the stream going.
+// 12 warps share an SM instead of 8 (at most 168 registers each), which the conversions of the
+// codes need to keep the stream going, with three stages each.
 template <int D, bool FP8 = false>
 struct DecodeCfg {
-  static constexpr int MAXW = 8;                      // warps (KV heads) per CTA, at most
-  static constexpr int NSW = 2;                       // ring stages per warp
+  static constexpr int MAXW = FP8 ? 12 : 8;           // warps per CTA, at most
+  static constexpr int NSW = FP8 ? 3 : 2;             // ring stages per warp
   static constexpr int WARPS_PER_SM = FP8 ? 12 : 8;   // resident warps per SM the launch aims for
   static constexpr int MAXREG = FP8 ? 168 : 255;      // registers per thread (12 warps per SM fit)
   static constexpr int BS = 16;                       // tokens per block
@@ -109,10 +111,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) __maxnreg__((Dec
   if (TB == 0) return;
 
   // ---- this CTA's share [b0, b1) of the blocks; this warp's KV head kh ----
-  const int nsh = active_shares(TB, gridDim.x, C::MIN_BLOCKS);
+  const int hw = p.share_warps, spc = nw / hw;
+  const int nsh = active_shares(TB, gridDim.x * spc, C::MIN_BLOCKS);
   const Shares sh(TB, nsh);
-  const int c = blockIdx.x;
-  const int kh = blockIdx.y * nw + warp;
+  const int c = blockIdx.x * spc + warp / hw;
+  const int kh = blockIdx.y * hw + warp % hw;
   if (c >= nsh || kh >= Hkv) return;  // warp-uniform; nothing below synchronises across warps
   const int64_t b0 = sh.start(c), b1 = sh.start(c + 1);
   if (b0 >= b1) return;
@@ -464,26 +467,44 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) __maxnreg__((Dec
 }
 
 // Largest dynamic shared memory a CTA of this kernel asks for: the device's opt-in limit per
-// block, less room for the kernel's few static shared variables.
-static int max_dyn_smem() { return max_smem_optin() - 1024; }
+// block, less room for the kernel's static shared variables (the merge state of up to 12 warps,
+// 1.2 KB).
+static int max_dyn_smem() { return max_smem_optin() - 2048; }
 
-// Launch shape: warps per CTA = KV heads per CTA (at most 8); about WARPS_PER_SM warps per SM,
-// as many CTAs as shared memory allows.
+// Launch shape. A CTA runs `spc` shares side by side, each with `hw` warps (one per KV head of
+// its group of heads): hw is the divisor of Hkv (at most MAXW) that puts the most warps on an SM
+// (ties to the larger), and about WARPS_PER_SM warps go to each SM, in as few CTAs as shared
+// memory allows (every CTA keeps its own copy of the set's tables).
 struct DecodeShape {
-  int nw, groups, shares;
+  int hw, spc, nw, groups, ctas_x, shares;
 };
 template <int D, bool FP8>
 static DecodeShape decode_shape(int Hkv) {
   using C = DecodeCfg<D, FP8>;
+  const int lim = max_dyn_smem();
   DecodeShape d;
-  d.nw = Hkv < C::MAXW ? Hkv : C::MAXW;
-  while (d.nw > 1 && C::smem(d.nw) > max_dyn_smem()) --d.nw;
-  d.groups = (Hkv + d.nw - 1) / d.nw;
+  d.hw = 1;
+  int best = 0;
+  for (int w = 1; w <= C::MAXW && w <= Hkv; ++w) {
+    if (Hkv % w != 0 && w != Hkv) continue;
+    if (C::smem(w) > lim) break;
+    const int per_sm = (C::WARPS_PER_SM / w > 0 ? C::WARPS_PER_SM / w : 1) * w;
+    if (per_sm >= best) {
+      best = per_sm;
+      d.hw = w;
+    }
+  }
+  d.spc = C::WARPS_PER_SM / d.hw > 0 ? C::WARPS_PER_SM / d.hw : 1;
+  while (d.spc * d.hw > C::MAXW) --d.spc;
+  while (d.spc > 1 && C::smem(d.spc * d.hw) > lim) --d.spc;
+  d.nw = d.spc * d.hw;
+  d.groups = (Hkv + d.hw - 1) / d.hw;
   int ctas_per_sm = C::WARPS_PER_SM / d.nw > 0 ? C::WARPS_PER_SM / d.nw : 1;
-  const int fit = (max_dyn_smem() + 1024) / (C::smem(d.nw) + 1024);
+  const int fit = (lim + 1024) / (C::smem(d.nw) + 1024);
   if (ctas_per_sm > fit) ctas_per_sm = fit > 0 ? fit : 1;
-  d.shares = num_sms() * ctas_per_sm / d.groups;
-  if (d.shares < 1) d.shares = 1;
+  d.ctas_x = num_sms() * ctas_per_sm / d.groups;
+  if (d.ctas_x < 1) d.ctas_x = 1;
+  d.shares = d.ctas_x * d.spc;
   return d;
 }
 // The most shares any decode launch of this head count uses (bf16 or FP8 cache).
@@ -513,8 +534,10 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
                                      FP8 ? kAttrDecode128Fp8 : (D == 64 ? kAttrDecode64 : kAttrDecode128));
   if (e != cudaSuccess) return e;
   const DecodeShape sh = decode_shape<D, FP8>(p.Hkv);
-  e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(sh.shares, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
-                 p, tk, tv);
+  DecodeParams q = p;
+  q.share_warps = sh.hw;
+  e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(sh.ctas_x, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
+                 q, tk, tv);
   *launches += 1;
   return e;
 }

@@ -37,6 +37,7 @@ struct DecodeParams {
   // the MLA decode one per slice of the value dims of a group of G query heads (out_dim = the
   // value width).
   int32_t units, out_dim;
+  int32_t share_warps;      // decode: warps of a CTA per share (its KV heads); CTA warps / share_warps shares per CTA
   const void* kv;           // MLA decode: the latent cache (blocks kv_block_bytes apart)
   int64_t kv_block_bytes;
 };

@@ -218,6 +218,20 @@ def test_decode_fp8_group_sizes(pkv, G):
     assert _errors(pkv) == 0
 
 
+@pytest.mark.parametrize("Hkv", [1, 3, 6, 8, 16])
+def test_decode_fp8_kv_head_counts(pkv, Hkv):
+    """The FP8 kernel's CTA layouts (12 warps a CTA: 12 one-warp shares at Hkv 1 and 3, 6 x 2 at
+    6, 3 x 4 at 8 and 16)."""
+    b, kc, vc, ks, vs = _fp8_decode_case(7, 1, 900, Hq=2 * Hkv, Hkv=Hkv, seed=400 + Hkv)
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), kc.to(DEV), vc.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(b.seq_lens_list), scale=1 / math.sqrt(128),
+                                     k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc), _codes(vc), b.block_tables.numpy(),
+                                           b.seq_lens.numpy(), 1 / math.sqrt(128), ks, vs)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode fp8 Hkv={Hkv}")
+    assert _errors(pkv) == 0
+
+
 @pytest.mark.parametrize("ctxs", [[1, 16, 17, 31, 32, 33], [4096, 1, 7000, 15]])
 def test_decode_fp8_edge_lengths_and_nan_codes_past_the_end(pkv, ctxs):
     """Ragged and cut sequences; codes past each sequence's end are NaN codes (0x7F), which
@@ -427,6 +441,22 @@ def test_decode_group_sizes(pkv, G, D):
     assert _errors(pkv) == 0
 
 
+@pytest.mark.parametrize("Hkv", [1, 3, 5, 6, 12, 16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_kv_head_counts(pkv, Hkv, D):
+    """KV head counts that lay the CTAs out differently: a CTA runs several shares side by side,
+    each with a divisor of Hkv as its warps (Hkv 3 and 5: one warp per share and one head group
+    per head; 6: two; 12 and 16: several head groups). Lengths cut sequences at share edges."""
+    b = gen.decode_batch(7, 1, 900, Hq=2 * Hkv, Hkv=Hkv, D=D, seed=300 + 7 * Hkv + D)
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                                     max(b.seq_lens_list), cu_q=g.cu_q, scale=scale)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"decode Hkv={Hkv} D={D}")
+    assert _errors(pkv) == 0
+
+
 def test_decode_tiny_config(pkv):
     """4 sequences, context U[16,200], 8 Q / 2 KV heads, head_dim 64, pool of 64 blocks, seed 0."""
     b = gen.decode_batch(**gen.TINY_DECODE)
@@ -456,7 +486,7 @@ def test_decode_edge_lengths_and_splits(pkv, ctxs):
 @pytest.mark.parametrize("ctxs", [[256], [640], [2048], [2176], [8320], [80000], [192000], [50000, 7, 30000]])
 def test_decode_long_sequences_merge_tree(pkv, ctxs):
     """A few long sequences spread over all the CTAs: each is cut into up to one piece per
-    share, and the pieces are merged along the fan-in-4 tree (depths 1 to 5 here, including
+    share, and the pieces are merged along the fan-in-4 tree (depths 1 to 6 here, including
     partly filled groups)."""
     b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=1, D=128, seed=sum(ctxs) % 101)
     g = b.to(DEV)

@@ -735,6 +735,15 @@ def profile_case(pkv, args):
         fn = lambda: pkv.extend_attn(b.q, b.k_new, b.v_new, b.cu_q, b.seq_lens, b.k_cache, b.v_cache,
                                      b.block_tables, 512, max(b.seq_lens_list))
         what = "extend 2 x (16000 cached + 512 new)"
+    elif args.profile == "extend_fp8":
+        # the extend case over an FP8 (E4M3) cache: the context gather (~530 MB of codes read
+        # and bf16 written per launch), then the scaled tensor-core kernel
+        b = gen.extend_batch([512, 512], [16000, 16000], Hq=64, Hkv=8, D=128, seed=3, device=dev)
+        ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+        kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+        fn = lambda: pkv.extend_attn(b.q, b.k_new, b.v_new, b.cu_q, b.seq_lens, kc, vc, b.block_tables, 512,
+                                     max(b.seq_lens_list), k_scale=ks, v_scale=vs)
+        what = "extend over an FP8 cache, 2 x (16000 cached + 512 new)"
     else:
         layers = gen.write_pack_layers(4, 10000, Hkv=8, D=128, seed=4, device=dev)
         def fn():
@@ -758,7 +767,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mla", "prefill", "extend", "write_pack"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mla", "prefill", "extend", "extend_fp8", "write_pack"], default=None,
                     help="run a reduced case of one kernel --steps times for an ncu capture; prints "
                          "a one-line summary, no benchmark line")
     args = ap.parse_args()

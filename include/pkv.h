@@ -12,7 +12,8 @@
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except where a
  *     comment says "host". The library allocates no device memory and keeps no state
- *     between calls other than one per-device error word (pkv_device_errors).
+ *     between calls other than one per-device error word (pkv_device_errors) and the
+ *     handoff handles the caller creates (pkv_handoff_create).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and returns after checking its host-side arguments and enqueueing its kernels. It
  *     never synchronises, except pkv_device_errors.
@@ -323,6 +324,44 @@ pkv_status pkv_kv_block_pack(pkv_cache cache, const int32_t* block_ids, int32_t 
  * ------------------------------------------------------------------------------------- */
 pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
                                pkv_cache cache, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Layer handoff staging — the per-layer pack of a prefill instance, overlapped with the work
+ * that follows it on the compute stream.
+ * Source: vLLM blog "moriio-kv-connector", section "Write mode": the prefill instance sends
+ * each layer's KV blocks as soon as that layer is done, so the transfer of one layer overlaps
+ * the compute of the next.
+ *
+ * A handle (host object, created and destroyed by the caller) holds a copy stream the caller
+ * chooses and, per staging slot, three CUDA events; no device memory. A slot stands for a
+ * staging buffer the caller owns and reuses (a ring of buffers).
+ *   pkv_handoff_create(num_slots, copy_stream, &h): num_slots >= 1 (host). copy_stream must
+ *     not be the compute stream the stages name (NULL is not accepted): the pack runs there.
+ *   pkv_handoff_stage(h, slot, cache, block_ids, num_ids, dst, compute_stream): the work
+ *     enqueued on compute_stream so far (the layer's kv_cache_write) is ordered before the
+ *     pack; the pack (the result of pkv_kv_block_pack: dst = [2][num_ids][block_size]
+ *     [num_kv_heads][head_dim]) runs on the copy stream after the slot's last release, if any;
+ *     work enqueued later on compute_stream does not wait for it. Its CTAs (128 threads, at
+ *     most 64 registers, no shared memory) fit beside a running attention kernel of this
+ *     library, so the copy overlaps it. The layer's cache blocks must not be written again
+ *     before the slot is ready.
+ *   pkv_handoff_ready(h, slot, stream): work enqueued on `stream` after this call waits for the
+ *     slot's last staged pack (the send of dst, or an unpack of it). Before any stage of the
+ *     slot it adds no wait.
+ *   pkv_handoff_release(h, slot, stream): the slot's next stage waits for the work enqueued on
+ *     `stream` so far (the consumer has finished reading dst).
+ *   pkv_handoff_destroy(h): frees the events and the handle; enqueued work still completes.
+ * Errors: PKV_ERR_INVALID_ARG for a NULL handle or output pointer, num_slots < 1, a slot
+ * outside [0, num_slots), a NULL copy stream, a call on a device other than the handle's, or
+ * what pkv_kv_block_pack rejects; PKV_ERR_CUDA when an event or stream call fails.
+ * ------------------------------------------------------------------------------------- */
+typedef struct pkv_handoff pkv_handoff;
+pkv_status pkv_handoff_create(int32_t num_slots, pkv_stream_t copy_stream, pkv_handoff** out);
+pkv_status pkv_handoff_stage(pkv_handoff* h, int32_t slot, pkv_cache cache, const int32_t* block_ids,
+                             int32_t num_ids, void* dst, pkv_stream_t compute_stream);
+pkv_status pkv_handoff_ready(pkv_handoff* h, int32_t slot, pkv_stream_t stream);
+pkv_status pkv_handoff_release(pkv_handoff* h, int32_t slot, pkv_stream_t stream);
+pkv_status pkv_handoff_destroy(pkv_handoff* h);
 
 /* ---------------------------------------------------------------------------------------
  * pkv_device_errors — read (and, if clear != 0, reset) the error word of the current device.

@@ -50,6 +50,11 @@ SIGNATURES = [
     ("pkv_varlen_prefill_attn", i32, [P, P, P, i64, P, PkvReqs, i32, i32, i32, i32, f32, P, P, P]),
     ("pkv_kv_block_pack", i32, [PkvCache, P, i32, P, P]),
     ("pkv_kv_block_unpack", i32, [P, P, i32, PkvCache, P]),
+    ("pkv_handoff_create", i32, [i32, P, P]),
+    ("pkv_handoff_stage", i32, [P, i32, PkvCache, P, i32, P, P]),
+    ("pkv_handoff_ready", i32, [P, i32, P]),
+    ("pkv_handoff_release", i32, [P, i32, P]),
+    ("pkv_handoff_destroy", i32, [P]),
     ("pkv_selftest_bounded_wait", i32, [ctypes.c_uint64, P]),
     ("pkv_device_errors", i32, [P, i32, P]),
     ("pkv_launch_count", i64, [i32]),

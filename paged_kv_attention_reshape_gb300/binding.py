@@ -121,6 +121,53 @@ def kv_block_unpack(src, block_ids, k_cache, v_cache, stream=None):
     _check(lib.pkv_kv_block_unpack(_ptr(src), _ptr(block_ids), n, cache, _stream(stream)), "kv_block_unpack")
 
 
+class LayerHandoff:
+    """Per-layer handoff staging on a copy stream of its own (pkv_handoff_*): stage(slot, ...)
+    packs one layer's blocks into dst after the work already on the compute stream, without
+    holding up the compute stream; ready(slot, stream) orders a consumer after that pack;
+    release(slot, stream) orders the slot's next stage after the consumer."""
+
+    def __init__(self, num_slots: int, copy_stream: Optional[torch.cuda.Stream] = None):
+        lib = _lib.load()
+        self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream()
+        self.num_slots = int(num_slots)
+        h = ctypes.c_void_p()
+        _check(lib.pkv_handoff_create(self.num_slots, _stream(self.copy_stream), ctypes.byref(h)), "handoff_create")
+        self._h = h
+
+    def stage(self, slot, k_cache, v_cache, block_ids, dst=None, compute_stream=None):
+        lib = _lib.load()
+        _need(block_ids, torch.int32, "block_ids")
+        cache = make_cache(k_cache, v_cache)
+        n = block_ids.numel()
+        if dst is None:
+            # allocated on the copy stream's behalf: the caching allocator must not hand it to
+            # other work before the pack that writes it is done
+            with torch.cuda.stream(self.copy_stream):
+                dst = torch.empty((2, n) + tuple(k_cache.shape[1:]), dtype=k_cache.dtype, device=k_cache.device)
+        _need(dst, k_cache.dtype, "dst")
+        _check(lib.pkv_handoff_stage(self._h, int(slot), cache, _ptr(block_ids), n, _ptr(dst), _stream(compute_stream)),
+               "handoff_stage")
+        return dst
+
+    def ready(self, slot, stream=None):
+        _check(_lib.load().pkv_handoff_ready(self._h, int(slot), _stream(stream)), "handoff_ready")
+
+    def release(self, slot, stream=None):
+        _check(_lib.load().pkv_handoff_release(self._h, int(slot), _stream(stream)), "handoff_release")
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _check(_lib.load().pkv_handoff_destroy(self._h), "handoff_destroy")
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def selftest_bounded_wait(limit_ns=10_000_000, stream=None):
     """Run a kernel whose barrier wait must run out after limit_ns (sets the TIMEOUT bit of the
     device error word; the context stays usable)."""

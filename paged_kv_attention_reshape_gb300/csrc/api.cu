@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "launch.h"
@@ -302,6 +303,109 @@ pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_
                                           reinterpret_cast<cudaStream_t>(stream)));
   t_launches += 1;
   return st;
+}
+
+}  // extern "C"
+
+// A layer handoff handle: the copy stream and, per slot, the events that order a stage after
+// the compute stream's writes (written), a consumer after the stage (staged) and the next stage
+// after the consumer (released).
+struct pkv_handoff {
+  int device;
+  int32_t slots;
+  cudaStream_t copy;
+  std::vector<cudaEvent_t> written, staged, released;
+  std::vector<char> has_release;
+};
+
+namespace {
+
+pkv_status handoff_slot_ok(const pkv_handoff* h, int32_t slot) {
+  if (h == nullptr || slot < 0 || slot >= h->slots) return PKV_ERR_INVALID_ARG;
+  const int d = current_device();
+  return d == h->device ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+void destroy_events(pkv_handoff* h) {
+  for (auto* v : {&h->written, &h->staged, &h->released})
+    for (cudaEvent_t e : *v)
+      if (e != nullptr) cudaEventDestroy(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_handoff_create(int32_t num_slots, pkv_stream_t copy_stream, pkv_handoff** out) {
+  if (out == nullptr || num_slots < 1 || num_slots > 4096 || copy_stream == nullptr) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int d = current_device();
+  if (d < 0) return PKV_ERR_CUDA;
+  auto* h = new pkv_handoff();
+  h->device = d;
+  h->slots = num_slots;
+  h->copy = reinterpret_cast<cudaStream_t>(copy_stream);
+  h->written.assign(num_slots, nullptr);
+  h->staged.assign(num_slots, nullptr);
+  h->released.assign(num_slots, nullptr);
+  h->has_release.assign(num_slots, 0);
+  for (auto* v : {&h->written, &h->staged, &h->released})
+    for (cudaEvent_t& e : *v)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        e = nullptr;
+        destroy_events(h);
+        delete h;
+        return PKV_ERR_CUDA;
+      }
+  *out = h;
+  return PKV_OK;
+}
+
+pkv_status pkv_handoff_stage(pkv_handoff* h, int32_t slot, pkv_cache cache, const int32_t* block_ids,
+                             int32_t num_ids, void* dst, pkv_stream_t compute_stream) {
+  pkv_status st = handoff_slot_ok(h, slot);
+  if (st != PKV_OK) return st;
+  const cudaStream_t compute = reinterpret_cast<cudaStream_t>(compute_stream);
+  if (compute == h->copy || num_ids < 0) return PKV_ERR_INVALID_ARG;
+  st = check_cache(cache, false);
+  if (st != PKV_OK) return st;
+  if (num_ids > 0) {
+    if (block_ids == nullptr || dst == nullptr || !aligned16(dst)) return PKV_ERR_INVALID_ARG;
+    if ((static_cast<int64_t>(cache.block_size) * cache.num_kv_heads * cache.head_dim * elem_bytes(cache)) % 16 != 0)
+      return PKV_ERR_UNSUPPORTED;
+    if (num_ids > 65535 * 1024) return PKV_ERR_UNSUPPORTED;
+  }
+  if (cudaEventRecord(h->written[slot], compute) != cudaSuccess ||
+      cudaStreamWaitEvent(h->copy, h->written[slot], 0) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (h->has_release[slot] && cudaStreamWaitEvent(h->copy, h->released[slot], 0) != cudaSuccess) return PKV_ERR_CUDA;
+  if (num_ids > 0) {
+    st = cuda_status(launch_kv_block_pack(cache, block_ids, num_ids, dst, error_word(), h->copy, true));
+    t_launches += 1;
+    if (st != PKV_OK) return st;
+  }
+  return cuda_status(cudaEventRecord(h->staged[slot], h->copy));
+}
+
+pkv_status pkv_handoff_ready(pkv_handoff* h, int32_t slot, pkv_stream_t stream) {
+  const pkv_status st = handoff_slot_ok(h, slot);
+  if (st != PKV_OK) return st;
+  return cuda_status(cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), h->staged[slot], 0));
+}
+
+pkv_status pkv_handoff_release(pkv_handoff* h, int32_t slot, pkv_stream_t stream) {
+  const pkv_status st = handoff_slot_ok(h, slot);
+  if (st != PKV_OK) return st;
+  if (cudaEventRecord(h->released[slot], reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+  h->has_release[slot] = 1;
+  return PKV_OK;
+}
+
+pkv_status pkv_handoff_destroy(pkv_handoff* h) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  destroy_events(h);
+  delete h;
+  return PKV_OK;
 }
 
 pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens,

@@ -1030,8 +1030,8 @@ def main():
                 "pack_hidden_frac": (m["serial"] - m["pipelined"]) / max(m["serial"] - m["no_pack"], 1e-9),
                 "pipelined_attn_tflops": r["flops"] / (m["pipelined"] * 1e-3) / 1e12,
                 "staged_buffers_match": r["staged_ok"],
-                "how": "pipelined: pkv_handoff_stage per layer on a copy stream (pack CTAs small enough to sit "
-                       "beside the attention kernel); serial: the same pack on the bench stream after the attention"}
+                "how": "pipelined: pkv_handoff_stage per layer on a copy stream; serial: the same pack on the "
+                       "bench stream after the attention"}
         except Exception as e:
             extras["handoff_pipeline"] = {"error": repr(e)}
         torch.cuda.empty_cache()

@@ -341,10 +341,9 @@ pkv_status pkv_kv_block_unpack(const void* src, const int32_t* block_ids, int32_
  *     enqueued on compute_stream so far (the layer's kv_cache_write) is ordered before the
  *     pack; the pack (the result of pkv_kv_block_pack: dst = [2][num_ids][block_size]
  *     [num_kv_heads][head_dim]) runs on the copy stream after the slot's last release, if any;
- *     work enqueued later on compute_stream does not wait for it. Its CTAs (128 threads, at
- *     most 64 registers, no shared memory) fit beside a running attention kernel of this
- *     library, so the copy overlaps it. The layer's cache blocks must not be written again
- *     before the slot is ready.
+ *     work enqueued later on compute_stream does not wait for it, so the copy can overlap
+ *     whatever runs there next (SMs permitting). The layer's cache blocks must not be written
+ *     again before the slot is ready.
  *   pkv_handoff_ready(h, slot, stream): work enqueued on `stream` after this call waits for the
  *     slot's last staged pack (the send of dst, or an unpack of it). Before any stage of the
  *     slot it adds no wait.

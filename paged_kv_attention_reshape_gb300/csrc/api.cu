@@ -380,7 +380,7 @@ pkv_status pkv_handoff_stage(pkv_handoff* h, int32_t slot, pkv_cache cache, cons
     return PKV_ERR_CUDA;
   if (h->has_release[slot] && cudaStreamWaitEvent(h->copy, h->released[slot], 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (num_ids > 0) {
-    st = cuda_status(launch_kv_block_pack(cache, block_ids, num_ids, dst, error_word(), h->copy, true));
+    st = cuda_status(launch_kv_block_pack(cache, block_ids, num_ids, dst, error_word(), h->copy));
     t_launches += 1;
     if (st != PKV_OK) return st;
   }

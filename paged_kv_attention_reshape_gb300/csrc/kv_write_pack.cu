@@ -129,13 +129,8 @@ __global__ void __launch_bounds__(256) kv_cache_write_fp8_kernel(
   }
 }
 
-// blockIdx.y selects K (0) or V (1); blockIdx.x is the destination block index i. THREADS =
-// 256 for a pack on its own; 128 (at most 64 registers) for a pack staged beside a running
-// attention kernel: one such CTA fits in what a tcgen05 attention CTA leaves of an SM (about
-// 11.5 K registers, 4.6 KB of shared memory), so the copy overlaps the attention instead of
-// waiting for its CTAs to leave.
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS, THREADS == 128 ? 8 : 1) kv_block_pack_kernel(
+// blockIdx.y selects K (0) or V (1); blockIdx.x is the destination block index i.
+__global__ void __launch_bounds__(256) kv_block_pack_kernel(
     const uint4* __restrict__ k_cache, const uint4* __restrict__ v_cache,
     const int32_t* __restrict__ block_ids, int32_t num_ids, int64_t num_blocks,
     int64_t block_stride_chunks, int64_t block_chunks, uint4* __restrict__ dst, unsigned int* err) {
@@ -221,15 +216,11 @@ cudaError_t launch_kv_cache_write(const void* key, const void* value, const int6
 }
 
 cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, int32_t num_ids,
-                                 void* dst, unsigned int* err, cudaStream_t stream, bool beside) {
+                                 void* dst, unsigned int* err, cudaStream_t stream) {
   const int64_t eb = elem_bytes(c);
   const int64_t block_chunks = static_cast<int64_t>(c.block_size) * c.num_kv_heads * c.head_dim * eb / 16;
   dim3 grid(num_ids, 2);
-  if (beside)
-    return launch_pdl(kv_block_pack_kernel<128>, grid, dim3(128), 0, stream, static_cast<const uint4*>(c.k),
-                      static_cast<const uint4*>(c.v), block_ids, num_ids, c.num_blocks, c.stride_block * eb / 16,
-                      block_chunks, static_cast<uint4*>(dst), err);
-  return launch_pdl(kv_block_pack_kernel<256>, grid, dim3(256), 0, stream, static_cast<const uint4*>(c.k),
+  return launch_pdl(kv_block_pack_kernel, grid, dim3(256), 0, stream, static_cast<const uint4*>(c.k),
                     static_cast<const uint4*>(c.v), block_ids, num_ids, c.num_blocks, c.stride_block * eb / 16,
                     block_chunks, static_cast<uint4*>(dst), err);
 }

@@ -129,9 +129,8 @@ int max_smem_optin();   // opt-in shared memory per block of the current device,
 cudaError_t launch_kv_cache_write(const void* key, const void* value, const int64_t* slot_mapping,
                                   int64_t num_tokens, const pkv_cache& c, unsigned int* err,
                                   cudaStream_t stream);
-// beside: the small-CTA shape that fits next to a running attention kernel (handoff staging)
 cudaError_t launch_kv_block_pack(const pkv_cache& c, const int32_t* block_ids, int32_t num_ids,
-                                 void* dst, unsigned int* err, cudaStream_t stream, bool beside = false);
+                                 void* dst, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_kv_block_unpack(const void* src, const int32_t* block_ids, int32_t num_ids,
                                    const pkv_cache& c, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_lens, int32_t R,

@@ -90,6 +90,12 @@ class Clocks:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout_s: float = 5.0):
+        """Wait until the sampler has printed its first line (nvidia-smi takes a moment to start)."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.02)
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -254,13 +260,23 @@ def decode_step(pkv, w, stream, marks=None, q=None, meta=None, k_new=None, v_new
         reqs=reqs, scale=1.0 / math.sqrt(b.D), out=out, lse=lse, workspace=w["ws"], stream=stream))
 
 
-def bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=0):
+def bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=0, hold_s=0.0, on_ready=None):
     """The headline step, timed whole; then the decode call alone (L2 flushed before each
-    launch, events right around it) for the kernel's launch duration."""
+    launch, events right around it) for the kernel's launch duration. on_ready runs once the
+    workload is built; hold_s more seconds of the same step follow the timing, untimed, so the
+    clock sampler sees the GPU under this load for longer than the timed steps last."""
     w = decode_workload(pkv, dev, seed_off)
+    if on_ready is not None:
+        on_ready()
     n0 = pkv.launch_count()
     ms, _ = timer.run(lambda m: decode_step(pkv, w, stream, m), steps, warmup, sections=False)
     launches = (pkv.launch_count() - n0) // (warmup + steps)
+    t_end = time.perf_counter() + hold_s
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            timer.flush()
+            decode_step(pkv, w, stream, None)
+        torch.cuda.synchronize()
     b, meta, R = w["b"], w["meta"], w["b"].R
     reqs = pkv.Reqs(max_reqs=R, batch_reqs=R, order=w["perm"], bounds=w["bounds"], cls=pkv.CLASS_DECODE)
     launch_ms, _ = timer.run(lambda m: pkv.paged_decode_attn(
@@ -869,7 +885,8 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        w, ms, sec, launches = bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=rank)
+        w, ms, sec, launches = bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=rank, hold_s=1.0,
+                                            on_ready=clocks.wait_first)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     step_ms = max_over_ranks(sum(ms) / len(ms), ws, dev)
@@ -912,8 +929,9 @@ def main():
                 "serial": {"value": replica_rate(w["kv_bytes"], ws, serial_step) / 1e9, "ms_per_step": serial_step,
                            "mode": "copy in, step, copy out, one stream, each step timed alone after an L2 flush"}},
         "gpu_launches": launches * steps,
-        "clocks": clocks.summary(),
-        "wall_s_timed": t_wall,
+        "clocks": dict(clocks.summary(), window="nvidia-smi every 200 ms from before the first warm-up step "
+                                                  "through the timed steps and 1 s more of the same step"),
+        "wall_s_decode_section": t_wall,
     }
     if not args.no_extras and rank == 0:
         extras = {}

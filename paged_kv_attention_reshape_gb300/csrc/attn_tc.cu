@@ -146,8 +146,12 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, vol
   return __all_sync(0xffffffffu, tc_wait(bar, parity, abort_flag, err));
 }
 
-// SCALED: the cached context holds the E4M3 values of an FP8 cache (gathered into bf16), whose
-// key and value scales apply per context tile; the bf16 cache's kernel has none of that code.
+// SCALED: the cached context holds the E4M3 values of an FP8 cache (gathered into bf16). The
+// key scale goes with the softmax scale of context tiles. The value scale vs is taken out of
+// the sum instead of multiplied into every context tile's P: the few new-token tiles pack
+// P / vs (2^(s - m - log2 vs): the same exponent with another shift; their row sum is scaled
+// back by vs), and the final normalisation multiplies O by vs, so that
+// O = vs * (sum_ctx p code + sum_new p v / vs) / l. The bf16 cache's kernel has none of it.
 template <int D, bool SCALED>
 __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
     const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t sc = 0, oc = 0;
     int odd = 0;
+    const float lvs = SCALED ? log2f(p.ctx_v_scale) : 0.f;  // new-token tiles' extra shift
     for (int64_t w = blockIdx.x; w < W; w = tc_next(w, odd)) {
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (slot >= it.nslot) continue;
@@ -288,10 +293,10 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
         const bool full = __all_sync(0xffffffffu, kv >= 128);
         const uint32_t srow = tmem + lane_off + scol(slot);
         // a context tile of an FP8 cache holds the E4M3 values themselves: its key scale goes
-        // with the softmax scale, its value scale onto P (the row sum stays unscaled)
+        // with the softmax scale; a new-token tile packs P / vs (the row sum stays unscaled)
         const bool ctx = j < it.nct;
         const float sl = SCALED && ctx ? p.ctx_scale_log2 : p.scale_log2;
-        const bool vsc = SCALED && ctx && p.ctx_v_scale != 1.f;
+        const bool vsc = SCALED && !ctx && p.ctx_v_scale != 1.f;
         // pass 1: row max of the raw scores (the scale is positive, so it commutes with max)
         float mx = -CUDART_INF_F;
 #pragma unroll
@@ -318,13 +323,12 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
           }
         }
         // pass 2: p = 2^(s * scale_log2 - m), packed to bf16 pairs over the first half of S
-        const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
+        const float neg_m = (m == -CUDART_INF_F ? 0.f : -m) - (vsc ? lvs : 0.f);
         float rs = 0.f;
         // every column valid: pairs of columns in packed fp32 (one instruction per pair for the
-        // scale-and-shift and the running sum); with a value scale, P is scaled as it is packed
-        auto full_pass = [&](auto scaled) {  // std::true_type: P scaled by the value scale
+        // scale-and-shift and the running sum)
+        auto full_pass = [&]() {
           const uint64_t sc2 = sm::f2(sl, sl), nm2 = sm::f2(neg_m, neg_m);
-          const uint64_t vs2 = sm::f2(p.ctx_v_scale, p.ctx_v_scale);
           uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -339,8 +343,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
               sm::unf2(x, x0, x1);
               const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
               rs2 = sm::add2(rs2, pp);
-              if constexpr (decltype(scaled)::value) pk[e / 2] = sm::bf16x2(sm::mul2(pp, vs2));
-              else pk[e / 2] = sm::bf16x2(pp);
+              pk[e / 2] = sm::bf16x2(pp);
             }
             tc::st16(srow + c * 16, pk);
           }
@@ -349,8 +352,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
           return r0 + r1;
         };
         if (full) {
-          if constexpr (SCALED) rs = vsc ? full_pass(std::true_type{}) : full_pass(std::false_type{});
-          else rs = full_pass(std::false_type{});
+          rs = full_pass();
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -365,12 +367,12 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
               p0 = (c * 32 + e < kv) ? p0 : 0.f;
               p1 = (c * 32 + e + 1 < kv) ? p1 : 0.f;
               rs += p0 + p1;
-              if constexpr (SCALED) pk[e / 2] = vsc ? pack_bf16(p0 * p.ctx_v_scale, p1 * p.ctx_v_scale) : pack_bf16(p0, p1);
-              else pk[e / 2] = pack_bf16(p0, p1);
+              pk[e / 2] = pack_bf16(p0, p1);
             }
             tc::st16(srow + c * 16, pk);
           }
         }
+        if (vsc) rs *= p.ctx_v_scale;  // the row sum of the unshifted p
         l = l * alpha + rs;
         // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole
         // warp takes the branch when any of its rows needs it (alpha is 1 for the others).
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
       const int h = it.h0 + slot;
       const int64_t row = it.row0 + qi;
       const bool write = t < it.nrows && row < p.num_tokens;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (SCALED ? p.ctx_v_scale : 1.f) / l : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

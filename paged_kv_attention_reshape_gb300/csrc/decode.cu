@@ -536,6 +536,7 @@ static cudaError_t launch_decode_impl(const DecodeParams& p, const CUtensorMap& 
   const DecodeShape sh = decode_shape<D, FP8>(p.Hkv);
   DecodeParams q = p;
   q.share_warps = sh.hw;
+  q.launch_shares = sh.shares;
   e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(sh.ctas_x, sh.groups), dim3(sh.nw * 32), C::smem(sh.nw), stream,
                  q, tk, tv);
   *launches += 1;

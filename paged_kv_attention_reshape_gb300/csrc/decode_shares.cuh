@@ -244,11 +244,12 @@ template <int D>
 __device__ __forceinline__ float* node_part(const DecodeParams& p, const Cut& s, int L, int a, int kh, int gg) {
   return p.ws_part + (((static_cast<int64_t>(s.share(L, a)) * 2 + s.slot(a)) * p.units + kh) * p.G + gg) * (D + 4);
 }
-// Arrival counter of node (L >= 1, a): [level - 1][share][slot][unit]. A share is the first
-// share of at most one cut sequence (slot 1) and holds the first piece of at most one (slot 0),
-// so no two nodes of a call share a counter.
+// Arrival counter of node (L >= 1, a): [level - 1][share][slot][unit], levels launch_shares
+// shares apart (every share of the launch, not one per CTA: a decode CTA runs several). A share
+// is the first share of at most one cut sequence (slot 1) and holds the first piece of at most
+// one (slot 0), so no two nodes of a call share a counter.
 __device__ __forceinline__ unsigned long long* node_ctr(const DecodeParams& p, const Cut& s, int L, int a, int kh) {
-  return p.ws_ctr + ((static_cast<int64_t>(L - 1) * gridDim.x + s.share(L, a)) * 2 + s.slot(a)) * p.units + kh;
+  return p.ws_ctr + ((static_cast<int64_t>(L - 1) * p.launch_shares + s.share(L, a)) * 2 + s.slot(a)) * p.units + kh;
 }
 // Counter levels a grid of `shares` CTAs needs: 4^levels >= shares.
 __host__ __device__ constexpr int merge_levels(int shares) {

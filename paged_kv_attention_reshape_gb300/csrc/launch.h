@@ -38,6 +38,7 @@ struct DecodeParams {
   // value width).
   int32_t units, out_dim;
   int32_t share_warps;      // decode: warps of a CTA per share (its KV heads); CTA warps / share_warps shares per CTA
+  int32_t launch_shares;    // shares the launch's grid holds (CTAs x shares per CTA): the level stride of the merge counters
   const void* kv;           // MLA decode: the latent cache (blocks kv_block_bytes apart)
   int64_t kv_block_bytes;
 };

@@ -428,8 +428,10 @@ cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cuda
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&mla_decode_kernel), MlaCfg::SMEM, kAttrMla);
   if (e != cudaSuccess) return e;
   const int groups = p.Hq / MlaCfg::HG;
-  e = launch_pdl(mla_decode_kernel, dim3(mla_shares(groups), groups), dim3(MlaCfg::THREADS), MlaCfg::SMEM, stream,
-                 p, tm);
+  DecodeParams q = p;
+  q.launch_shares = mla_shares(groups);  // one share per CTA
+  e = launch_pdl(mla_decode_kernel, dim3(q.launch_shares, groups), dim3(MlaCfg::THREADS), MlaCfg::SMEM, stream,
+                 q, tm);
   *launches += 1;
   return e;
 }

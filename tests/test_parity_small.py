@@ -498,6 +498,34 @@ def test_decode_long_sequences_merge_tree(pkv, ctxs):
     assert _errors(pkv) == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("ctxs", [[80000], [192000], [50000, 7, 30000]])
+def test_decode_long_sequences_several_shares_per_cta(pkv, ctxs, fp8):
+    """Long sequences at a head count where one CTA runs several shares side by side (Hkv 4:
+    2 shares of 4 warps a CTA for a bf16 cache, 3 for FP8), so the launch holds more shares
+    than CTAs: the merge counters of different tree levels must still be distinct (levels are
+    a whole launch's shares apart). Each call is repeated, since counters shared by two nodes
+    would only go wrong when their arrivals interleave."""
+    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=4, D=128,
+                       seed=sum(ctxs) % 97)
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    kw, kc, vc = {}, g.k_cache, g.v_cache
+    if fp8:
+        ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+        kc8, vc8 = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+        kw, kc, vc = dict(k_scale=ks, v_scale=vs), kc8.to(DEV), vc8.to(DEV)
+        ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc8), _codes(vc8), b.block_tables.numpy(),
+                                               b.seq_lens.numpy(), scale, ks, vs)
+    else:
+        ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    for rep in range(4):
+        out, lse = pkv.paged_decode_attn(g.q, kc, vc, g.block_tables, g.seq_lens, max(ctxs), cu_q=g.cu_q,
+                                         scale=scale, **kw)
+        compare_attention(out, lse, ref, ref_lse, what=f"decode long {ctxs} fp8={fp8} call {rep}")
+    assert _errors(pkv) == 0
+
+
 def test_decode_peaked_softmax(pkv):
     b = gen.decode_batch(8, 100, 900, Hq=32, Hkv=4, D=128, seed=77, q_scale=4.0)
     g = b.to(DEV)

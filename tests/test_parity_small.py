@@ -498,16 +498,23 @@ def test_decode_long_sequences_merge_tree(pkv, ctxs):
     assert _errors(pkv) == 0
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("ctxs", [[80000], [192000], [50000, 7, 30000]])
-def test_decode_long_sequences_several_shares_per_cta(pkv, ctxs, fp8):
-    """Long sequences at a head count where one CTA runs several shares side by side (Hkv 4:
-    2 shares of 4 warps a CTA for a bf16 cache, 3 for FP8), so the launch holds more shares
-    than CTAs: the merge counters of different tree levels must still be distinct (levels are
-    a whole launch's shares apart). Each call is repeated, since counters shared by two nodes
-    would only go wrong when their arrivals interleave."""
-    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=16, Hkv=4, D=128,
-                       seed=sum(ctxs) % 97)
+@pytest.mark.parametrize("Hq,Hkv,D,fp8,longs,seed", [
+    (64, 4, 128, True, [83746], 3),           # FP8, 3 shares of 4 warps a CTA (the headline shape)
+    (64, 4, 128, True, [150633, 60000], 7),
+    (64, 4, 128, False, [120000], 11),        # bf16, 2 shares of 4 warps a CTA
+    (24, 6, 64, False, [153387], 10),         # bf16 D 64 at Hkv 6
+    (16, 4, 128, False, [192000], 5),
+])
+def test_decode_long_sequences_several_shares_per_cta(pkv, Hq, Hkv, D, fp8, longs, seed):
+    """Long sequences (cut into hundreds of pieces) among short ones, at head counts where one
+    CTA runs several shares side by side, so the launch holds more shares than CTAs: the merge
+    counters of different tree levels must be distinct (levels a whole launch's shares apart).
+    Counters shared by two nodes only go wrong when their arrivals interleave, so every call is
+    repeated."""
+    rnd = np.random.default_rng(seed)
+    ctxs = list(longs) + [int(x) for x in rnd.integers(0, 3000, size=int(rnd.integers(8, 30)))]
+    rnd.shuffle(ctxs)
+    b = gen.make_batch([gen.DECODE] * len(ctxs), [1] * len(ctxs), ctxs, Hq=Hq, Hkv=Hkv, D=D, seed=seed)
     g = b.to(DEV)
     scale = default_scale(b.D)
     kw, kc, vc = {}, g.k_cache, g.v_cache
@@ -519,10 +526,10 @@ def test_decode_long_sequences_several_shares_per_cta(pkv, ctxs, fp8):
                                                b.seq_lens.numpy(), scale, ks, vs)
     else:
         ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
-    for rep in range(4):
+    for rep in range(6):
         out, lse = pkv.paged_decode_attn(g.q, kc, vc, g.block_tables, g.seq_lens, max(ctxs), cu_q=g.cu_q,
                                          scale=scale, **kw)
-        compare_attention(out, lse, ref, ref_lse, what=f"decode long {ctxs} fp8={fp8} call {rep}")
+        compare_attention(out, lse, ref, ref_lse, what=f"decode long Hq {Hq} Hkv {Hkv} D {D} fp8={fp8} call {rep}")
     assert _errors(pkv) == 0
 
 

@@ -285,6 +285,48 @@ def test_extend_fp8_ragged(pkv, G, D):
     assert _errors(pkv) == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_shared_prefix_blocks(pkv, fp8):
+    """Prefix reuse: the block tables of several requests point at the same physical blocks
+    for a common prefix (60 whole blocks, 960 tokens), as a prefix cache hands them out. Decode
+    and extend read the shared blocks in place (the FP8 extend gathers them once per request);
+    the results equal the oracle's over the same tables."""
+    kinds = [gen.DECODE] * 4 + [gen.EXTEND] * 3
+    q_lens = [1, 1, 1, 1, 40, 200, 129]
+    seq_lens = [2000, 1500, 3100, 2049, 1840, 2700, 1329]
+    b = gen.make_batch(kinds, q_lens, seq_lens, Hq=32, Hkv=4, D=128, seed=123)
+    bt = b.block_tables.clone()
+    bt[1:, :60] = bt[0, :60]
+    b.block_tables = bt
+    g = b.to(DEV)
+    scale = default_scale(b.D)
+    kw, kc, vc = {}, g.k_cache, g.v_cache
+    if fp8:
+        ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+        kc8, vc8 = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+        kw, kc, vc = dict(k_scale=ks, v_scale=vs), kc8.to(DEV), vc8.to(DEV)
+    dec = pkv.Reqs(max_reqs=4, batch_reqs=b.R)  # requests 0..3
+    ext = pkv.Reqs(max_reqs=3, batch_reqs=b.R, order=torch.tensor([4, 5, 6], dtype=torch.int32, device=DEV))
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((b.T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_attn(g.q, kc, vc, g.block_tables, g.seq_lens, max(seq_lens), cu_q=g.cu_q, reqs=dec,
+                          scale=scale, out=out, lse=lse, **kw)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kc, vc, g.block_tables, max(q_lens), max(seq_lens),
+                    reqs=ext, scale=scale, out=out, lse=lse, **kw)
+    assert _errors(pkv) == 0
+    ref = np.full((b.T, b.Hq, b.D), np.nan)
+    ref_lse = np.full((b.T, b.Hq), np.nan)
+    if fp8:
+        oracle.paged_decode_fp8(bits(b.q), _codes(kc8), _codes(vc8), bt.numpy(), b.seq_lens.numpy(), scale, ks, vs,
+                                cu_q=b.cu_q.numpy(), req_ids=[0, 1, 2, 3], out=ref, lse=ref_lse)
+        _fp8_extend_ref(b, _codes(kc8), _codes(vc8), ks, vs, scale, req_ids=[4, 5, 6], out=ref, lse=ref_lse)
+    else:
+        oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale, req_ids=[0, 1, 2, 3], out=ref, lse=ref_lse)
+        oracle_extend(b, bits(b.k_cache), bits(b.v_cache), scale, req_ids=[4, 5, 6], out=ref, lse=ref_lse)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, what=f"shared prefix fp8={fp8}")
+
+
 def test_extend_fp8_request_set_and_peaked(pkv):
     """A request set from the reorder's outputs over a shuffled batch, peaked queries, and
     NaN codes past the end of each context (never gathered into a sum)."""

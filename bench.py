@@ -39,9 +39,21 @@ from pkv_workloads import gen  # noqa: E402
 L2_FLUSH_BYTES = 512 << 20
 
 
-HEADLINE_WORKLOAD = ("decode-only Qwen3-235B-like attention layer: 256 seqs, ctx U[2000,3000], "
-                     "Hq 64 / Hkv 4, head_dim 128, block 16, pool 1.2x, shuffled blocks; "
-                     "step = reorder + kv_cache_write + paged_decode_attn")
+HEADLINE_WORKLOAD = "qwen3-235b-like decode layer: 256 seqs ctx U[2000,3000] Hq64/Hkv4 D128 bs16 bf16; reorder+write+decode"
+
+
+def headline_config(kv_bytes: int, ws: int) -> dict:
+    """The workload description both arms (GPU and --impl reference) print, key for key."""
+    return {"workload": HEADLINE_WORKLOAD, "kv_bytes_per_step": kv_bytes,
+            "l2": "inputs larger than L2 (1.3 GB KV per step); the GPU arm also writes 512 MiB between timed steps",
+            "parallelism": f"replicas x{ws}"}
+
+
+def _r(x, n=4):
+    """x rounded to n significant digits (keeps the JSON line short)."""
+    if x is None or not isinstance(x, (int, float)) or x == 0 or not math.isfinite(x):
+        return x
+    return float(f"{x:.{n}g}")
 
 
 def dist_env():
@@ -289,6 +301,24 @@ def bench_decode(pkv, dev, stream, timer, steps, warmup, seed_off=0, hold_s=0.0,
         scale=1.0 / math.sqrt(b.D), out=w["out"], lse=w["lse"], workspace=w["ws"], stream=stream),
         max(steps, 20), warmup, sections=False)
     return w, ms, {"decode": launch_ms}, launches
+
+
+def bench_tiny_decode(pkv, dev, stream, timer, steps, warmup):
+    """The tiny paged decode (4 sequences, context U[16,200], Hq 8 / Hkv 2, D 64, a 64-block
+    pool): one decode call, L2 flushed before it. Latency-bound; its GB/s is informational."""
+    b = gen.decode_batch(**gen.TINY_DECODE, device=dev)
+    maxs = max(b.seq_lens_list)
+    kv = sum(b.seq_lens_list) * b.Hkv * b.D * 2 * 2
+    out = torch.empty_like(b.q)
+    lse = torch.empty((b.R, b.Hq), dtype=torch.float32, device=dev)
+    ws_n = pkv.paged_decode_workspace_size(b.R, b.Hq, b.Hkv, b.D, maxs)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    meta = dict(cu_q=b.cu_q.to(dev), seq_lens=b.seq_lens.to(dev), block_tables=b.block_tables.to(dev))
+    ms, _ = timer.run(lambda m: pkv.paged_decode_attn(
+        b.q, b.k_cache, b.v_cache, meta["block_tables"], meta["seq_lens"], maxs, cu_q=meta["cu_q"],
+        scale=1.0 / math.sqrt(b.D), out=out, lse=lse, workspace=ws, stream=stream), steps, warmup, sections=False)
+    t = sorted(ms)[len(ms) // 2]
+    return {"kv_bytes": kv, "launch_ms": t, "kv_gbs": kv / (t * 1e-3) / 1e9}
 
 
 def bench_decode_fp8(pkv, dev, stream, timer, steps, warmup):
@@ -723,17 +753,27 @@ def bench_handoff(pkv, dev, stream, timer, steps, warmup):
             pkv.kv_cache_write(L.key, L.value, L.slot_mapping, L.k_cache, L.v_cache, stream=stream)
             pkv.varlen_prefill_attn(q, L.key, L.value, cu, T, out=out, stream=stream)
 
-    res = {}
-    for name, fn in (("serial", serial), ("pipelined", pipelined), ("no_pack", alone)):
-        ms, _ = timer.run(fn, steps, warmup, sections=False)
-        res[name] = sorted(ms)[len(ms) // 2]
+    # five rounds, the three modes interleaved in each, so that the spread between rounds shows
+    # whether the difference between modes is above the noise
+    rounds = {"serial": [], "pipelined": [], "no_pack": []}
+    for _ in range(5):
+        for name, fn in (("serial", serial), ("pipelined", pipelined), ("no_pack", alone)):
+            ms, _ = timer.run(fn, steps, warmup if not rounds[name] else 1, sections=False)
+            rounds[name].append(sorted(ms)[len(ms) // 2])
     torch.cuda.synchronize()
+    med = {k: statistics.median(v) for k, v in rounds.items()}
+    saved = [a - b for a, b in zip(rounds["serial"], rounds["pipelined"])]
     ok = True
     for L, d in zip(layers[:2], dsts[:2]):  # the staged buffers hold the layers' blocks
         ok &= bool(torch.equal(d[0], L.k_cache[L.block_ids.long()])) and bool(torch.equal(d[1], L.v_cache[L.block_ids.long()]))
     ho.close()
     del layers, dsts
-    return dict(ms=res, flops=flops, staged_ok=ok)
+    packs = [a - b for a, b in zip(rounds["serial"], rounds["no_pack"])]
+    return {"serial_ms": med["serial"], "pipelined_ms": med["pipelined"], "without_pack_ms": med["no_pack"],
+            "rounds_ms": {k: [_r(x) for x in v] for k, v in rounds.items()},
+            "saved_ms_median": statistics.median(saved), "saved_ms_range": [_r(min(saved)), _r(max(saved))],
+            "pack_cost_ms_median": statistics.median(packs),
+            "pipelined_attn_tflops": flops / (med["pipelined"] * 1e-3) / 1e12, "staged_buffers_match": ok}
 
 
 # ---- CPU oracle ---------------------------------------------------------------------------------
@@ -864,11 +904,9 @@ def main():
                 "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic",
-                "config": {"workload": HEADLINE_WORKLOAD,
-                           "kv_bytes_per_step": sum(b.seq_lens_list) * b.Hkv * b.D * 2 * 2,
-                           "parallelism": "replicas x1 (rank 0 only)",
-                           "oracle_step": "the fp64 oracle's decode of whole requests of this batch; the reorder "
-                                          "and the write are index copies it does not time"},
+                "config": headline_config(sum(b.seq_lens_list) * b.Hkv * b.D * 2 * 2, args.gpus),
+                "oracle_step": "the fp64 oracle's decode of whole requests of this batch (rank 0 only); the "
+                               "reorder and the write are index copies it does not time",
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -917,51 +955,46 @@ def main():
         "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": HEADLINE_WORKLOAD,
-                   "kv_bytes_per_step": w["kv_bytes"], "l2": "512 MiB buffer written between timed steps; "
-                   "KV read per step (1.3 GB) is also larger than L2", "parallelism": f"replicas x{ws}"},
-        "roofline": {"kernel": "paged_decode_kernel (+ split merge)", "bound": "hbm", "achieved": achieved,
+        "config": headline_config(w["kv_bytes"], ws),
+        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": w["alg_bytes"],
                      "peak_source": peaks["source"] + " (hbm copy, burst)", "launch_ms": dec_ms,
-                     "launch_timing": f"mean of {len(sec['decode'])} decode calls on the bench stream, each "
-                                      "alone between CUDA events, L2 flushed before each"},
-        "frac_of_nominal_8TBs": w["kv_bytes"] / (dec_ms * 1e-3) / 8e12,
-        "e2e": {"value": replica_rate(w["kv_bytes"], ws, e2e_step) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
-                "steps": e2e_steps,
-                "mode": "pipelined: each step copies its inputs host-to-device and reads out/lse back, "
-                        "on copy streams with double buffers, overlapping the neighbouring steps' kernels "
-                        "(as asynchronous scheduling in a serving engine); device time of the whole run / steps",
-                "serial": {"value": replica_rate(w["kv_bytes"], ws, serial_step) / 1e9, "ms_per_step": serial_step,
-                           "mode": "copy in, step, copy out, one stream, each step timed alone after an L2 flush"}},
+                     "launch_timing": f"mean of {len(sec['decode'])} lone decode calls, CUDA events, L2 flushed"},
+        "e2e": {"value": replica_rate(w["kv_bytes"], ws, serial_step) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": serial_step,
+                "steps": len(e2e_ms),
+                "mode": "serial: copy in, step, copy out on one stream, each step alone after an L2 flush",
+                "pipelined_value": replica_rate(w["kv_bytes"], ws, e2e_step) / 1e9,
+                "pipelined_ms_per_step": e2e_step},
         "gpu_launches": launches * steps,
-        "clocks": dict(clocks.summary(), window="nvidia-smi every 200 ms from before the first warm-up step "
-                                                  "through the timed steps and 1 s more of the same step"),
-        "wall_s_decode_section": t_wall,
+        "clocks": dict(clocks.summary(), window="nvidia-smi every 200 ms, first warm-up step to 1 s past the timed steps"),
     }
+    summary = {"decode_frac_of_measured_hbm": _r(achieved / peaks["hbm"]),
+               "decode_frac_of_nominal_8TBs": _r(w["kv_bytes"] / (dec_ms * 1e-3) / 8e12),
+               "e2e_serial_gbs": _r(line["e2e"]["value"]), "e2e_pipelined_gbs": _r(line["e2e"]["pipelined_value"])}
     if not args.no_extras and rank == 0:
         extras = {}
         try:
             m = bench_mixed(pkv, dev, stream, timer, steps, warmup)
             mms = sum(m["ms"]) / len(m["ms"])
-            per = {k: sum(v) / len(v) for k, v in m["sec"].items()}
+            per = {k: _r(sum(v) / len(v)) for k, v in m["sec"].items()}
+            ums = sum(m["unified_ms"]) / len(m["unified_ms"])
+            bound = (m["dec_bytes"] / (peaks["hbm"] * 1e9) + (m["ext_flops"] + m["pre_flops"]) /
+                     (peaks["bf16_sust"] * 1e12)) * 1e3
             extras["mixed_batch"] = {
-                "workload": "Llama-3.1-70B-like layer (Hq 64 / Hkv 8, D 128): 192 decode ctx U[1000,8000], "
-                            "8 extend 512 new over U[4000,32000] cached, 4 prefill U[2000,8000], shuffled",
                 "tokens_per_s": m["tokens"] / (mms * 1e-3), "ms_per_step": mms, "tokens": m["tokens"],
                 "per_call_ms": per, "gpu_launches_per_step": m["launches"],
                 "decode_kv_gbs": m["dec_bytes"] / (per["decode"] * 1e-3) / 1e9,
                 "extend_tflops": m["ext_flops"] / (per["extend"] * 1e-3) / 1e12,
                 "prefill_tflops": m["pre_flops"] / (per["prefill"] * 1e-3) / 1e12,
-                "bound_ms": (m["dec_bytes"] / (peaks["hbm"] * 1e9) + (m["ext_flops"] + m["pre_flops"]) /
-                             (peaks["bf16_sust"] * 1e12)) * 1e3,
-            }
-            extras["mixed_batch"]["frac_of_bound"] = extras["mixed_batch"]["bound_ms"] / mms
-            ums = sum(m["unified_ms"]) / len(m["unified_ms"])
-            extras["mixed_batch"]["unified_single_call"] = {
-                "what": "write + one extend_attn over all requests in arrival order (no reorder, no routing)",
-                "ms_per_step": ums, "tokens_per_s": m["tokens"] / (ums * 1e-3)}
+                "bound_ms": bound, "frac_of_bound": bound / mms,
+                "unified_single_call": {"ms_per_step": ums, "tokens_per_s": m["tokens"] / (ums * 1e-3)}}
+            summary.update(mixed_tokens_per_s=_r(m["tokens"] / (mms * 1e-3)), mixed_ms=_r(mms),
+                           mixed_frac_of_bound=_r(bound / mms),
+                           mixed_prefill_frac=_r(extras["mixed_batch"]["prefill_tflops"] / peaks["bf16"]),
+                           mixed_extend_frac=_r(extras["mixed_batch"]["extend_tflops"] / peaks["bf16"]),
+                           unified_tokens_per_s=_r(m["tokens"] / (ums * 1e-3)))
             del m
         except Exception as e:  # report, keep the headline
             extras["mixed_batch"] = {"error": repr(e)}
@@ -970,47 +1003,41 @@ def main():
             m8 = bench_mixed_fp8(pkv, dev, stream, timer, steps, warmup)
             mms8 = sum(m8["ms"]) / len(m8["ms"])
             extras["mixed_batch_fp8"] = {
-                "workload": "the mixed batch over an FP8 (E4M3, per-tensor scale) cache: quantising write, "
-                            "decode dequantising as it reads, extend through the gather of its context into bf16",
                 "tokens_per_s": m8["tokens"] / (mms8 * 1e-3), "ms_per_step": mms8,
-                "per_call_ms": {k: sum(v) / len(v) for k, v in m8["sec"].items()},
+                "per_call_ms": {k: _r(sum(v) / len(v)) for k, v in m8["sec"].items()},
                 "extend_workspace_bytes": m8["ws_bytes"], "device_errors": m8["errors"],
             }
+            summary.update(fp8_mixed_tokens_per_s=_r(m8["tokens"] / (mms8 * 1e-3)))
         except Exception as e:
             extras["mixed_batch_fp8"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             r = bench_decode_fp8(pkv, dev, stream, timer, steps, warmup)
+            fr = r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"]
             extras["decode_fp8"] = {
-                "workload": "the headline decode step over an FP8 (E4M3, per-tensor scale) cache: 256 seqs, "
-                            "ctx U[2000,3000], Hq 64 / Hkv 4, D 128; step = reorder + quantising kv_cache_write "
-                            "+ paged_decode_attn",
                 "kv_bytes_per_step": r["kv_bytes"], "ms_per_step": r["step_ms"],
                 "kv_gbs": r["kv_bytes"] / (r["step_ms"] * 1e-3) / 1e9,
                 "decode_tokens_per_s": r["R"] / (r["step_ms"] * 1e-3),
                 "bf16_decode_tokens_per_s": w["b"].R / (step_ms * 1e-3),
-                "launch_ms": r["launch_ms"],
-                "roofline_frac": r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"],
+                "launch_ms": r["launch_ms"], "roofline_frac": fr,
             }
+            summary.update(fp8_decode_frac=_r(fr), fp8_decode_tokens_per_s=_r(r["R"] / (r["step_ms"] * 1e-3)))
         except Exception as e:
             extras["decode_fp8"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             r = bench_mla(pkv, dev, stream, timer, steps, warmup)
+            fr = r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"]
             extras["mla_decode"] = {
-                "workload": "DeepSeek-R1-like MLA layer, tensor parallel 8: 128 seqs, ctx U[10000,11000], "
-                            "Hq 16 over one 576-wide latent (values = first 512 dims), block 16; step = "
-                            "kv_cache_write of the new latent rows + mla_decode_attn",
                 "latent_bytes_per_step": r["lat_bytes"], "ms_per_step": r["step_ms"],
                 "latent_gbs": r["lat_bytes"] / (r["step_ms"] * 1e-3) / 1e9,
                 "decode_tokens_per_s": r["R"] / (r["step_ms"] * 1e-3),
-                "launch_ms": r["launch_ms"],
-                "roofline_frac": r["alg_bytes"] / (r["launch_ms"] * 1e-3) / 1e9 / peaks["hbm"],
+                "launch_ms": r["launch_ms"], "roofline_frac": fr,
                 "mma_tflops": r["flops"] / (r["launch_ms"] * 1e-3) / 1e12,
                 "traffic": profiled_traffic("mla_decode", "mla_deepseek_tp8"),
-                "algorithmic_bytes_per_launch": r["alg_bytes"],
-                "device_errors": r["errors"],
+                "algorithmic_bytes_per_launch": r["alg_bytes"], "device_errors": r["errors"],
             }
+            summary.update(mla_decode_frac=_r(fr))
         except Exception as e:
             extras["mla_decode"] = {"error": repr(e)}
         torch.cuda.empty_cache()
@@ -1021,42 +1048,36 @@ def main():
                 k = "prefill" if kind == "prefill" else "extend"
                 t = sum(r["sec"][k]) / len(r["sec"][k])
                 tf = r["flops"] / (t * 1e-3) / 1e12
-                extras[kind] = {"workload": "4 x 8192 prompts, Hq 64 / Hkv 8, D 128" if kind == "prefill"
-                                else "2 x (100000 cached + 2048 new), Hq 64 / Hkv 8, D 128, budget 32768",
-                                "tflops": tf, "ms": t, "frac_of_bf16_peak": tf / peaks["bf16"],
+                extras[kind] = {"tflops": tf, "ms": t, "frac_of_bf16_peak": tf / peaks["bf16"],
                                 "peak_tflops": peaks["bf16"], "peak_source": peaks["source"] + " (bf16 burst)"}
+                summary[f"{kind}_tflops"] = _r(tf)
+                summary[f"{kind}_frac"] = _r(tf / peaks["bf16"])
             except Exception as e:
                 extras[kind] = {"error": repr(e)}
             torch.cuda.empty_cache()
         try:
             r = bench_write_pack(pkv, dev, stream, timer, max(3, steps // 2), warmup)
-            tw = sum(r["sec"]["write"]) / len(r["sec"]["write"])
-            tp = sum(r["sec"]["pack"]) / len(r["sec"]["pack"])
-            tu = sum(r["sec"]["unpack"]) / len(r["sec"]["unpack"])
-            extras["write_pack"] = {"workload": "80 layers x 10000 tokens, Hkv 8, D 128 (320 KiB/token); "
-                                                "each layer packed, then landed in a receiving pool",
-                                    "write_gbs": r["write_bytes"] / (tw * 1e-3) / 1e9,
-                                    "pack_gbs": r["pack_bytes"] / (tp * 1e-3) / 1e9,
-                                    "write_ms_80_layers": tw, "pack_ms_80_layers": tp,
-                                    "write_frac": r["write_bytes"] / (tw * 1e-3) / 1e9 / peaks["hbm"],
-                                    "pack_frac": r["pack_bytes"] / (tp * 1e-3) / 1e9 / peaks["hbm"],
-                                    "unpack_gbs": r["unpack_bytes"] / (tu * 1e-3) / 1e9, "unpack_ms_80_layers": tu,
-                                    "unpack_frac": r["unpack_bytes"] / (tu * 1e-3) / 1e9 / peaks["hbm"]}
+            res = {}
+            for k in ("write", "pack", "unpack"):
+                t = sum(r["sec"][k]) / len(r["sec"][k])
+                res[f"{k}_gbs"] = r[f"{k}_bytes"] / (t * 1e-3) / 1e9
+                res[f"{k}_ms_80_layers"] = t
+                res[f"{k}_frac"] = res[f"{k}_gbs"] / peaks["hbm"]
+                summary[f"{k}_frac"] = _r(res[f"{k}_frac"])
+            extras["write_pack"] = res
         except Exception as e:
             extras["write_pack"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
-            r = bench_handoff(pkv, dev, stream, timer, max(3, steps // 3), warmup)
-            m = r["ms"]
-            extras["handoff_pipeline"] = {
-                "workload": "prefill instance, 80 Llama-3.1-70B-like layers: write the 10000-token prompt's K/V, "
-                            "causal prefill attention (Hq 64 / Hkv 8), pack the layer's 625 blocks",
-                "serial_ms": m["serial"], "pipelined_ms": m["pipelined"], "without_pack_ms": m["no_pack"],
-                "pack_hidden_frac": (m["serial"] - m["pipelined"]) / max(m["serial"] - m["no_pack"], 1e-9),
-                "pipelined_attn_tflops": r["flops"] / (m["pipelined"] * 1e-3) / 1e12,
-                "staged_buffers_match": r["staged_ok"],
-                "how": "pipelined: pkv_handoff_stage per layer on a copy stream; serial: the same pack on the "
-                       "bench stream after the attention"}
+            r = bench_tiny_decode(pkv, dev, stream, timer, max(steps, 20), warmup)
+            extras["tiny_decode"] = r
+            summary["tiny_decode_gbs"] = _r(r["kv_gbs"])
+        except Exception as e:
+            extras["tiny_decode"] = {"error": repr(e)}
+        try:
+            r = bench_handoff(pkv, dev, stream, timer, max(3, steps // 4), warmup)
+            extras["handoff_pipeline"] = r
+            summary["handoff_saved_ms"] = _r(r["saved_ms_median"])
         except Exception as e:
             extras["handoff_pipeline"] = {"error": repr(e)}
         torch.cuda.empty_cache()
@@ -1064,6 +1085,7 @@ def main():
     if rank == 0:
         if ws == 1:
             line["cpu_baseline"] = oracle_decode_rate(w["b"], budget_s=args.oracle_seconds)
+        line["summary"] = summary  # last: the key numbers of every row in the line's final characters
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -58,12 +58,18 @@
  *   pkv_batch_classify_reorder) the set is order[bounds[cls] .. bounds[cls+1]-1]; a set
  *   larger than max_reqs is cut to max_reqs and flags PKV_DEVERR_REQS. So the three
  *   attention calls can follow the on-device reorder without a host round trip.
+ *   One kernel launch holds 1024 requests of a set in shared memory; a call whose max_reqs is
+ *   larger enqueues ceil(max_reqs / 1024) launches, each over the next 1024 positions of the
+ *   set (a launch whose positions lie past the set's actual size exits at once), so sets of
+ *   any size up to the call's limit are served in full.
  *
  * Supported shapes (anything else returns PKV_ERR_UNSUPPORTED; there is no fallback path):
  *   head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}; block_size 16 for the
  *   attention calls (kv_cache_write and kv_block_pack take any block_size >= 1). The MLA
  *   decode takes one 576-wide latent head, 512 value dims and 16 to 128 query heads in
- *   groups of 16.
+ *   groups of 16. Request sets: reqs.max_reqs <= 65535 for the decode and MLA calls (larger
+ *   returns PKV_ERR_UNSUPPORTED), any int32 for prefill and for extend over a bf16 cache,
+ *   <= 1024 for extend over an FP8 cache (its context gather holds one pool per request).
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -181,9 +187,10 @@ pkv_status pkv_batch_classify_reorder(const int32_t* cu_q, const int32_t* seq_le
  * sets PKV_DEVERR_LEN and the request is cut to the bound.
  * workspace: device buffer of at least pkv_paged_decode_workspace_size(...) bytes with the
  * same reqs.max_reqs, num_q_heads, head_dim, max_seq_len and cache (it holds the split-KV
- * partials and their arrival counters); its contents need no initialisation (every call tags
- * its counters with a value of its own); may be NULL when that size is 0. Calls that share a
- * workspace must not overlap.
+ * partials and their arrival counters); its contents need no initialisation (every launch tags
+ * its counters with a value of its own, in a bit pattern that no stored partial takes, so
+ * neither earlier counters nor earlier partials of another shape pass for this launch's
+ * counters); may be NULL when that size is 0. Calls that share a workspace must not overlap.
  * ------------------------------------------------------------------------------------- */
 size_t pkv_paged_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim,
@@ -205,12 +212,13 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
  * Its split-KV scratch is one array of PKV_NOALLOC_SCRATCH_BYTES bytes compiled into the
  * library as a device variable: every GPU that loads the library's device code holds that
  * memory until the process exits. The first call on a device looks up the array's device
- * address (with that device current) and caches it; make that first call before any stream
- * capture. A call whose scratch need, pkv_paged_decode_workspace_size(...) with the same
+ * address (with that device current) and caches it with the id of the CUDA context current
+ * then; a later call that finds another context current (after cudaDeviceReset, say) looks it
+ * up again. Make that first call before any stream capture. A call whose scratch need, pkv_paged_decode_workspace_size(...) with the same
  * arguments, exceeds PKV_NOALLOC_SCRATCH_BYTES returns PKV_ERR_WORKSPACE and enqueues
  * nothing. All calls on a device share the one array and it keeps the last call's contents;
  * nothing in it has to start at zero (each call writes every partial it later reads and tags
- * its arrival counters with a value of its own), but
+ * its arrival counters with a value of its own that no leftover partial or counter matches), but
  * calls that overlap on the GPU (other streams, other host threads) race on it: serialise
  * them.
  * ------------------------------------------------------------------------------------- */

@@ -480,12 +480,17 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   p.ws_part = static_cast<float*>(workspace);
   p.ws_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
                                                    decode_workspace_ctr_offset(p.Hq, p.Hkv, cache.head_dim));
-  p.epoch = next_epoch();
   CUtensorMap tk, tv;
   if (!encode_cache(&tk, cache.k, cache) || !encode_cache(&tv, cache.v, cache)) return PKV_ERR_CUDA;
+  // one launch per chunk of kSetChunk set positions, in stream order (each reuses the
+  // workspace after the previous one has completed), each with an epoch of its own
   int launches = 0;
-  st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim, fp8,
-                                       reinterpret_cast<cudaStream_t>(stream), &launches));
+  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
+    p.set_offset = off;
+    p.epoch = next_epoch();
+    st = cuda_status(launch_paged_decode(p, tk, tv, cache.head_dim, fp8,
+                                         reinterpret_cast<cudaStream_t>(stream), &launches));
+  }
   t_launches += launches;
   return st;
 }
@@ -546,11 +551,14 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
   p.ws_part = static_cast<float*>(workspace);
   p.ws_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
                                                    mla_workspace_ctr_offset(num_q_heads));
-  p.epoch = next_epoch();
   CUtensorMap tm;
   if (!encode_cache(&tm, cache.k, cache)) return PKV_ERR_CUDA;
   int launches = 0;
-  st = cuda_status(launch_mla_decode(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches));
+  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
+    p.set_offset = off;
+    p.epoch = next_epoch();
+    st = cuda_status(launch_mla_decode(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches));
+  }
   t_launches += launches;
   return st;
 }
@@ -616,8 +624,11 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
       (!encode_cache(&tck, cache->k, *cache) || !encode_cache(&tcv, cache->v, *cache)))
     return PKV_ERR_CUDA;
   int launches = 0;
-  st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D,
-                                    reinterpret_cast<cudaStream_t>(stream), &launches));
+  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
+    p.set_offset = off;
+    st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D,
+                                      reinterpret_cast<cudaStream_t>(stream), &launches));
+  }
   t_launches += launches;
   return st;
 }

@@ -44,7 +44,7 @@ struct TcCfg {
   static constexpr int HALF_BYTES = 128 * 128;           // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile of Q, K or V
   static constexpr int NBUF = D == 128 ? 4 : 8;           // K/V ring: one tile per buffer
-  static constexpr int MAXR = 1024;                       // requests per set (work list)
+  static constexpr int MAXR = kSetChunk;                  // requests of the set one launch holds
   static constexpr int THREADS = 320;
   static constexpr int RING_OFF = 2 * TILE_BYTES;
   static constexpr int REQ_OFF = RING_OFF + NBUF * TILE_BYTES;  // int4 {r, row0, q_len, C}
@@ -66,6 +66,8 @@ struct TcItem {
   int64_t row0;
 };
 
+// This launch's chunk of the request set: positions [begin, begin + n), the set's positions
+// set_offset .. set_offset + kSetChunk - 1 that exist.
 __device__ __forceinline__ void tc_resolve_set(const AttnParams& p, int& begin, int& n) {
   begin = 0;
   n = p.max_reqs;
@@ -75,6 +77,9 @@ __device__ __forceinline__ void tc_resolve_set(const AttnParams& p, int& begin, 
     if (n > p.max_reqs) n = p.max_reqs;
     if (n < 0) n = 0;
   }
+  begin += p.set_offset;
+  n = min(n - p.set_offset, kSetChunk);
+  if (n < 0) n = 0;
 }
 
 // Work item w (all roles walk the same sequence of items); s_req holds {request id, first
@@ -185,9 +190,8 @@ __global__ void __launch_bounds__(320, 1) attention_tc_kernel(
   tc_resolve_set(p, begin, n);
   if (blockIdx.x == 0 && tid == 0) {
     if (p.bounds != nullptr && p.bounds[p.cls + 1] - p.bounds[p.cls] > p.max_reqs) flag_error(p.err, PKV_DEVERR_REQS);
-    if (n > C::MAXR) flag_error(p.err, PKV_DEVERR_REQS);
   }
-  if (n > C::MAXR) n = C::MAXR;
+  static_assert(C::MAXR >= kSetChunk, "a launch holds a whole chunk of the set");
 
   if (tid == 0) {
     mbar_init(q_full, 1);

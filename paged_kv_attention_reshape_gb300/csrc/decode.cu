@@ -57,7 +57,7 @@ struct DecodeCfg {
   static constexpr int TILE_BYTES = BS * D * EB;      // one block of K (or V) for one head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
   static constexpr int Q_BYTES = 16 * D * 2;
-  static constexpr int MAXR = 1024;     // requests per set handled on device
+  static constexpr int MAXR = kSetChunk;  // requests of the set one launch holds
   static constexpr int MIN_BLOCKS = 8;  // smallest share (blocks) a CTA is given
   static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;  // s_pre[MAXR+1], s_ctx, s_r, s_row
   // per-warp region: ring [NSW][K | V], Q [half][16][64], barriers
@@ -90,9 +90,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, FP8>::MAXW * 32) __maxnreg__((Dec
   resolve_set(p, begin, n);
   if (blockIdx.x == 0 && tid == 0) {
     if (p.bounds != nullptr && p.bounds[p.cls + 1] - p.bounds[p.cls] > p.max_reqs) flag_error(p.err, PKV_DEVERR_REQS);
-    if (n > C::MAXR) flag_error(p.err, PKV_DEVERR_REQS);
   }
-  if (n > C::MAXR) n = C::MAXR;
+  static_assert(C::MAXR >= kSetChunk, "a launch holds a whole chunk of the set");
   const int cap = min(p.max_seq_len, p.max_blocks * C::BS);
   const int carry = static_cast<int>(scan_set<C::BS>(p.order, p.seq_lens, p.cu_q, begin, n, p.batch_reqs, cap,
                                                      p.err, s_pre, s_ctx, s_r, s_row, s_scan));

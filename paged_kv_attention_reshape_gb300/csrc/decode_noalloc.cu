@@ -10,8 +10,12 @@
 // The array is a file-scope __device__ object: every GPU that loads this code holds
 // PKV_NOALLOC_SCRATCH_BYTES of device memory for it until the process exits. Host code only
 // knows the array by a host-side stand-in symbol, so its device address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current (on the first call made
-// on that device), and the looked-up address is what the kernels receive.
+// cudaGetSymbolAddress, with the device current, on the first call made on that device (the
+// set-up), and the looked-up address is what the kernels receive. The address belongs to the
+// CUDA context that was current then; it is kept together with that context's id and looked
+// up again when a call finds another context current (after cudaDeviceReset, say).
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "launch.h"
@@ -22,18 +26,45 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PKV_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 
+// Id of the context current on this thread (driver API, found through the runtime), or 0 when
+// it cannot be read, in which case the address is looked up on every call.
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 // Device address of g_decode_scratch on the current device, or NULL if the lookup failed.
 void* scratch_on_current_device() {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || p == nullptr) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }

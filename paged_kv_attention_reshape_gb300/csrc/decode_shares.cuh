@@ -23,7 +23,8 @@ __device__ __forceinline__ int64_t out_offset(const DecodeParams& p, int64_t row
   return (row * p.Hq + out_head<UPG>(p, kh, gg)) * static_cast<int64_t>(OUT_DIM) + (kh % UPG) * D;
 }
 
-// Resolve the request set: [begin, begin + n) of `order` (or of the identity).
+// Resolve this launch's chunk of the request set: positions [begin, begin + n) of `order` (or
+// of the identity), the set's positions set_offset .. set_offset + kSetChunk - 1 that exist.
 __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, int& n) {
   begin = 0;
   n = p.max_reqs;
@@ -33,6 +34,9 @@ __device__ __forceinline__ void resolve_set(const DecodeParams& p, int& begin, i
     if (n > p.max_reqs) n = p.max_reqs;
     if (n < 0) n = 0;
   }
+  begin += p.set_offset;
+  n = min(n - p.set_offset, kSetChunk);
+  if (n < 0) n = 0;
 }
 
 // The set's sequences into shared memory (every CTA, redundantly): per position i < n, the
@@ -108,9 +112,8 @@ __device__ __forceinline__ int64_t load_set(const DecodeParams& p, int begin, in
   const int tid = threadIdx.x, nthreads = blockDim.x;
   if (blockIdx.x == 0 && tid == 0) {
     if (p.bounds != nullptr && p.bounds[p.cls + 1] - p.bounds[p.cls] > p.max_reqs) flag_error(p.err, PKV_DEVERR_REQS);
-    if (n > MAXR) flag_error(p.err, PKV_DEVERR_REQS);
   }
-  if (n > MAXR) n = MAXR;
+  static_assert(MAXR >= kSetChunk, "a launch holds a whole chunk of the set");
   const int cap = min(p.max_seq_len, p.max_blocks * BS);
   const int64_t total = scan_set<BS>(p.order, p.seq_lens, p.cu_q, begin, n, p.batch_reqs, cap, p.err, s_pre, s_ctx,
                                      s_r, s_row, s_scan);
@@ -196,12 +199,19 @@ struct PieceIter {
   }
 };
 
-// Arrival counters of cut sequences hold epoch << 32 | count. A counter whose epoch is not this
-// call's, or whose count is not below the sequence's piece count, was left by an earlier call
-// and counts as empty.
+// Arrival counters of cut sequences hold epoch << 32 | kCtrTag | count (count < 256). A counter
+// whose epoch is not this call's, whose tag is missing, or whose count is not below the node's
+// child count, was left by an earlier call (or is other data: a workspace reused at another
+// shape may hold fp32 partials where this call's counters lie) and counts as empty. The tag
+// makes the low word a signalling-NaN bit pattern, which no arithmetic result takes (the GPU's
+// NaN results are the canonical quiet NaN), so a stale pair of partial floats never passes for
+// a counter, whatever the epoch has wrapped to.
+constexpr uint32_t kCtrTag = 0x7FA5A500u;
 __device__ __forceinline__ uint32_t arrivals_of(unsigned long long v, uint32_t epoch, int total) {
-  const uint32_t cnt = static_cast<uint32_t>(v);
-  return (static_cast<uint32_t>(v >> 32) != epoch || cnt >= static_cast<uint32_t>(total)) ? 0u : cnt;
+  const uint32_t lo = static_cast<uint32_t>(v), cnt = lo & 0xFFu;
+  return (static_cast<uint32_t>(v >> 32) != epoch || (lo & ~0xFFu) != kCtrTag || cnt >= static_cast<uint32_t>(total))
+             ? 0u
+             : cnt;
 }
 // Count one arrival, starting from `cur`, the counter's value as last read. Returns the
 // arrivals so far, this one included, or 0 if the update kept failing.
@@ -209,7 +219,7 @@ __device__ __forceinline__ int arrive_counter(unsigned long long* ctr, uint32_t 
                                               unsigned long long cur, unsigned int* err) {
   for (int it = 0; it < (1 << 16); ++it) {
     const uint32_t cnt = arrivals_of(cur, epoch, total);
-    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | kCtrTag | (cnt + 1u);
     const unsigned long long prev = atomicCAS(ctr, cur, want);
     if (prev == cur) return static_cast<int>(cnt + 1u);
     cur = prev;

@@ -11,6 +11,12 @@
 
 namespace pkv {
 
+// Requests one launch of a decode, MLA decode or attention kernel holds in shared memory. A
+// larger set is served by consecutive launches over set positions [k * kSetChunk, (k + 1) *
+// kSetChunk) (set_offset = k * kSetChunk); the host knows only the set's bound max_reqs, so it
+// issues ceil(max_reqs / kSetChunk) launches and a launch whose chunk is empty exits at once.
+constexpr int kSetChunk = 1024;
+
 struct DecodeParams {
   unsigned int* err;  // device error word
   const __nv_bfloat16* q;
@@ -25,6 +31,7 @@ struct DecodeParams {
   int32_t cls;
   int32_t max_reqs;
   int32_t batch_reqs;
+  int32_t set_offset;    // first set position of this launch's chunk (a multiple of kSetChunk)
   int32_t Hq, Hkv, G;
   int64_t num_blocks;
   int32_t max_seq_len;
@@ -58,6 +65,7 @@ struct AttnParams {
   int32_t cls;
   int32_t max_reqs;
   int32_t batch_reqs;
+  int32_t set_offset;           // first set position of this launch's chunk (a multiple of kSetChunk)
   int32_t Hq, Hkv, G;
   int64_t num_blocks;
   int64_t num_tokens;           // rows of q / k_new / v_new

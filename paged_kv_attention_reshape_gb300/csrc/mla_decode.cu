@@ -55,7 +55,7 @@ struct MlaCfg {
   static constexpr int Q_ROW = KW * 2 + 16;      // 304: a query slice row, padded off the banks
   static constexpr int Q_BYTES = HG * Q_ROW;     // per compute warp
   static constexpr int XCHG_BYTES = NCW * 16 * 24 * 4 + 16 * 48;  // partial scores, then P
-  static constexpr int MAXR = 1024;              // requests per set handled on device
+  static constexpr int MAXR = kSetChunk;         // requests of the set one launch holds
   static constexpr int MIN_BLOCKS = 8;           // smallest share a CTA is given
   static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;
   static constexpr int OFF_Q = NS * STAGE_BYTES;

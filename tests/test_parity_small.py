@@ -815,3 +815,73 @@ def test_request_set_cut_to_max_reqs_is_flagged(pkv):
                           reqs=reqs, out=out)
     assert _errors(pkv) & 0x4
     assert out[4:].abs().sum().item() == 0  # requests past the bound are not computed
+
+
+# ---- request sets larger than one launch holds (1024 requests) -------------------------------
+
+def test_decode_request_sets_larger_than_one_launch(pkv):
+    """1500 short decode sequences: more than the 1024 requests one launch holds, so two launches
+    serve them. Every row against the oracle; once as the plain set, once as the decode class of
+    a reordered batch whose size the host only bounds (max_reqs 2048), in a shuffled order."""
+    R = 1500
+    b = gen.decode_batch(R, 1, 300, Hq=16, Hkv=2, D=128, seed=1500)
+    g = b.to(DEV)
+    scale = default_scale(128)
+    ref, ref_lse = oracle_decode(b, bits(b.k_cache), bits(b.v_cache), scale)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((g.T, g.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, max(b.seq_lens_list),
+                          cu_q=g.cu_q, scale=scale, out=out, lse=lse)
+    compare_attention(out, lse, ref, ref_lse, what="decode 1500 requests")
+    assert _errors(pkv) == 0
+    order = torch.randperm(R, generator=torch.Generator().manual_seed(3)).to(torch.int32)
+    bounds = torch.tensor([0, R, R, R], dtype=torch.int32)
+    reqs = pkv.Reqs(max_reqs=2048, batch_reqs=R, order=order.to(DEV), bounds=bounds.to(DEV), cls=0)
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    pkv.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens, max(b.seq_lens_list),
+                          cu_q=g.cu_q, reqs=reqs, scale=scale, out=out, lse=lse)
+    compare_attention(out, lse, ref, ref_lse, what="decode 1500 requests, reordered set")
+    assert _errors(pkv) == 0
+
+
+def test_decode_fp8_request_set_larger_than_one_launch(pkv):
+    b, kc, vc, ks, vs = _fp8_decode_case(1100, 1, 200, Hq=32, Hkv=4, seed=1100)
+    out, lse = pkv.paged_decode_attn(b.q.to(DEV), kc.to(DEV), vc.to(DEV), b.block_tables.to(DEV),
+                                     b.seq_lens.to(DEV), max(b.seq_lens_list), scale=1 / math.sqrt(128),
+                                     k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle.paged_decode_fp8(bits(b.q), _codes(kc), _codes(vc), b.block_tables.numpy(),
+                                           b.seq_lens.numpy(), 1 / math.sqrt(128), ks, vs)
+    compare_attention(out, lse, ref, ref_lse, what="decode fp8 1100 requests")
+    assert _errors(pkv) == 0
+
+
+def test_mla_decode_request_set_larger_than_one_launch(pkv):
+    b = gen.mla_batch(1100, 1, 120, Hq=16, seed=1101)
+    out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
+    compare_attention(out, lse, ref, ref_lse, what="mla 1100 requests")
+    assert _errors(pkv) == 0
+
+
+def test_prefill_and_extend_request_sets_larger_than_one_launch(pkv):
+    """1100 short prompts (prefill), and 1030 short extends: each needs two launches."""
+    lens = gen.uniform_ints(1, 40, 1100, torch.Generator().manual_seed(1102))
+    b = gen.prefill_batch(lens, Hq=8, Hkv=2, D=64, seed=1102)
+    g = b.to(DEV)
+    scale = default_scale(64)
+    out, lse = pkv.varlen_prefill_attn(g.q, g.k_new, g.v_new, g.cu_q, max(lens), scale=scale)
+    ref, ref_lse = oracle_prefill(b, scale)
+    compare_attention(out, lse, ref, ref_lse, what="prefill 1100 requests")
+    assert _errors(pkv) == 0
+    gr = torch.Generator().manual_seed(1103)
+    new = gen.uniform_ints(1, 20, 1030, gr)
+    ctx = gen.uniform_ints(1, 60, 1030, gr)
+    b = gen.extend_batch(new, ctx, Hq=8, Hkv=2, D=128, seed=1103)
+    g = b.to(DEV)
+    scale = default_scale(128)
+    out, lse = pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, g.k_cache, g.v_cache,
+                               g.block_tables, max(new), max(b.seq_lens_list), scale=scale)
+    ref, ref_lse = oracle_extend(b, bits(b.k_cache), bits(b.v_cache), scale)
+    compare_attention(out, lse, ref, ref_lse, what="extend 1030 requests")
+    assert _errors(pkv) == 0

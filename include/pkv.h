@@ -38,7 +38,8 @@
  *   ("gather_and_maybe_dequant_cache"); its served models are FP8. kv_cache_write stores
  *   E4M3(float(x) * (1.0f / scale)), rounded to the nearest code (ties to even) and saturated
  *   at +-448; pack/unpack copy codes; paged_decode_attn dequantises as it reads (head_dim 128);
- *   extend_attn gathers the set's context into a bf16 pool of the E4M3 values first (see
+ *   extend_attn reads the codes and converts them on chip (head_dim 128), or gathers the set's
+ *   context into a bf16 pool of the E4M3 values first (head_dim 64; see
  *   pkv_extend_fp8_workspace_size).
  *
  * The batch (arrival order, the layout vLLM's model runner gives its attention backend)
@@ -58,18 +59,18 @@
  *   pkv_batch_classify_reorder) the set is order[bounds[cls] .. bounds[cls+1]-1]; a set
  *   larger than max_reqs is cut to max_reqs and flags PKV_DEVERR_REQS. So the three
  *   attention calls can follow the on-device reorder without a host round trip.
- *   One kernel launch holds 1024 requests of a set in shared memory; a call whose max_reqs is
- *   larger enqueues ceil(max_reqs / 1024) launches, each over the next 1024 positions of the
- *   set (a launch whose positions lie past the set's actual size exits at once), so sets of
- *   any size up to the call's limit are served in full.
+ *   One kernel launch holds 1024 requests of a set (decode, MLA) or 256 (extend, prefill) in
+ *   shared memory; a call whose max_reqs is larger enqueues ceil(max_reqs / that) launches,
+ *   each over the next positions of the set (a launch whose positions lie past the set's
+ *   actual size exits at once), so sets of any size up to the call's limit are served in full.
  *
  * Supported shapes (anything else returns PKV_ERR_UNSUPPORTED; there is no fallback path):
  *   head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}; block_size 16 for the
  *   attention calls (kv_cache_write and kv_block_pack take any block_size >= 1). The MLA
  *   decode takes one 576-wide latent head, 512 value dims and 16 to 128 query heads in
  *   groups of 16. Request sets: reqs.max_reqs <= 65535 for the decode and MLA calls (larger
- *   returns PKV_ERR_UNSUPPORTED), any int32 for prefill and for extend over a bf16 cache,
- *   <= 1024 for extend over an FP8 cache (its context gather holds one pool per request).
+ *   returns PKV_ERR_UNSUPPORTED), any int32 for prefill and extend, except extend over an FP8
+ *   cache at head_dim 64, <= 1024 (its context gather holds one pool per request).
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -272,12 +273,17 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
  * chunk_budget_tokens: the context chunk budget (0 = whole context as one chunk); results do
  * not depend on it. The partials of the chunks are merged by LSE inside the kernel.
  * workspace: for a bf16 cache it may be NULL (none is needed; pkv_extend_workspace_size
- * returns 0). For an FP8 (E4M3) cache it must hold at least pkv_extend_fp8_workspace_size(
- * reqs.max_reqs, reqs.batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim) bytes
- * (else PKV_ERR_WORKSPACE): the context of the set's requests is gathered there as bf16
- * (the MLA section's "gather and maybe dequant" of the cached context), exactly the E4M3
- * values, and the scales are applied in the attention (keys with the softmax scale, values on
- * the softmax weights); head_dim 64 or 128. The workspace is rewritten by every such call.
+ * returns 0). For an FP8 (E4M3) cache at head_dim 128 it may be NULL as well: the kernel
+ * loads the context's codes (half the bytes of bf16) and converts them in shared memory to
+ * fp16, which holds every E4M3 value exactly (the MLA section's "maybe dequant" of the cached
+ * context, done on chip); the products then run on fp16 operands, so the queries, the new
+ * keys and the new values divided by v_scale must lie within the fp16 range (|x| < 65504).
+ * At head_dim 64 it must hold at least pkv_extend_fp8_workspace_size(reqs.max_reqs,
+ * reqs.batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim) bytes (else
+ * PKV_ERR_WORKSPACE): the context of the set's requests is gathered there as bf16 (the MLA
+ * section's "gather and maybe dequant"), exactly the E4M3 values. Either way the scales are
+ * applied in the attention (keys with the softmax scale, values on the output). The workspace
+ * is rewritten by every such call.
  * ------------------------------------------------------------------------------------- */
 size_t pkv_extend_workspace_size(int32_t max_reqs, int32_t max_q_len, int32_t num_q_heads,
                                  int32_t head_dim, int32_t chunk_budget_tokens);

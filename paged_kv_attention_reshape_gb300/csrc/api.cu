@@ -68,6 +68,12 @@ uint32_t next_epoch() {
   return e;
 }
 
+// The extend/prefill kernel's work-item counter slot of the next launch (process-wide, in turn).
+int32_t next_sched_slot() {
+  static std::atomic<uint32_t> seq{0};
+  return static_cast<int32_t>(seq.fetch_add(1, std::memory_order_relaxed) % kAttnSchedSlots);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t elem_bytes(const pkv_cache& c) { return c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2; }
@@ -566,19 +572,21 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
 size_t pkv_extend_workspace_size(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 // Extend (cache != NULL) and prefill (cache == NULL) share the checks and the kernel.
-// ctx_k_scale / ctx_v_scale: scales of the cached context's keys and values (1 for a bf16
-// cache; an FP8 context arrives here as a bf16 pool of the E4M3 values themselves).
+// ctx_kind: the cache is bf16 (kAttnCtxBf16), a bf16 pool holding the E4M3 values of an FP8
+// cache (kAttnCtxPool), or the FP8 cache itself, read as codes (kAttnCtxFp8, head_dim 128).
+// ctx_k_scale / ctx_v_scale: scales of the cached context's keys and values (1 for a bf16 cache).
 static pkv_status run_attention(const void* q, const void* k, const void* v, int64_t num_tokens,
                                 const int32_t* cu_q, const int32_t* seq_lens,
                                 const pkv_cache* cache, const int32_t* block_tables,
                                 int32_t max_blocks, pkv_reqs reqs, int32_t Hq, int32_t Hkv,
                                 int32_t D, int32_t max_q_len, int32_t max_seq_len, float scale,
-                                void* out, float* lse, pkv_stream_t stream, float ctx_k_scale = 1.f,
-                                float ctx_v_scale = 1.f) {
+                                void* out, float* lse, pkv_stream_t stream, int ctx_kind = kAttnCtxBf16,
+                                float ctx_k_scale = 1.f, float ctx_v_scale = 1.f) {
   pkv_status st = check_reqs(reqs);
   if (st != PKV_OK) return st;
   if (cache != nullptr && (st = check_cache(*cache, true)) != PKV_OK) return st;
-  if (cache != nullptr && cache->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (cache != nullptr && cache->kv_dtype != (ctx_kind == kAttnCtxFp8 ? PKV_KV_FP8_E4M3 : PKV_KV_BF16))
+    return PKV_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   if (!group_ok(Hq, Hkv)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale))
@@ -624,9 +632,10 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
       (!encode_cache(&tck, cache->k, *cache) || !encode_cache(&tcv, cache->v, *cache)))
     return PKV_ERR_CUDA;
   int launches = 0;
-  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
+  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kAttnSetChunk) {
     p.set_offset = off;
-    st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D,
+    p.sched_slot = next_sched_slot();
+    st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D, cache != nullptr ? ctx_kind : kAttnCtxBf16,
                                       reinterpret_cast<cudaStream_t>(stream), &launches));
   }
   t_launches += launches;
@@ -659,6 +668,7 @@ size_t pkv_extend_fp8_workspace_size(int32_t max_reqs, int32_t batch_reqs, int32
                                      int32_t max_blocks, int32_t num_kv_heads, int32_t head_dim) {
   if (max_reqs < 0 || batch_reqs < 0 || max_seq_len < 0 || max_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
     return 0;
+  if (head_dim == 128) return 0;  // the kernel converts the codes itself
   return fp8_extend_layout(max_reqs, batch_reqs, max_seq_len, max_blocks, num_kv_heads, head_dim).bytes;
 }
 
@@ -673,8 +683,14 @@ pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, 
     return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &cache, block_tables,
                          max_blocks, reqs, num_q_heads, cache.num_kv_heads, cache.head_dim,
                          max_q_len, max_seq_len, scale, out, lse, stream);
-  // FP8 cache: gather the set's context into a bf16 pool of the E4M3 values, then the bf16
-  // kernel over that pool with the scales applied per context tile
+  // FP8 cache, head_dim 128: the kernel loads the context's codes and converts them in shared
+  // memory (no workspace)
+  if (cache.head_dim == 128)
+    return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &cache, block_tables, max_blocks, reqs,
+                         num_q_heads, cache.num_kv_heads, cache.head_dim, max_q_len, max_seq_len, scale, out, lse,
+                         stream, kAttnCtxFp8, cache.k_scale, cache.v_scale);
+  // FP8 cache, head_dim 64: gather the set's context into a bf16 pool of the E4M3 values, then
+  // the kernel over that pool with the scales applied per context tile
   pkv_status st = check_cache(cache, false);
   if (st != PKV_OK) return st;
   if ((st = check_reqs(reqs)) != PKV_OK) return st;
@@ -726,8 +742,8 @@ pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, 
   pool.kv_dtype = PKV_KV_BF16;
   pool.k_scale = pool.v_scale = 1.f;
   return run_attention(q, k_new, v_new, num_tokens, cu_q, seq_lens, &pool, g.table_out, max_blocks, reqs,
-                       num_q_heads, Hkv, D, max_q_len, max_seq_len, scale, out, lse, stream, cache.k_scale,
-                       cache.v_scale);
+                       num_q_heads, Hkv, D, max_q_len, max_seq_len, scale, out, lse, stream, kAttnCtxPool,
+                       cache.k_scale, cache.v_scale);
 }
 
 pkv_status pkv_varlen_prefill_attn(const void* q, const void* k, const void* v, int64_t num_tokens,

@@ -107,6 +107,18 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// ---- 16-byte shared-memory accesses by 32-bit shared address ----------------------------------
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // ---- cp.async (16-byte global -> shared copies, per thread) -----------------------------------
 // Copies src_bytes (0 or 16) from src and zero-fills the rest of the 16 bytes at dst.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {

@@ -16,6 +16,12 @@ namespace pkv {
 // kSetChunk) (set_offset = k * kSetChunk); the host knows only the set's bound max_reqs, so it
 // issues ceil(max_reqs / kSetChunk) launches and a launch whose chunk is empty exits at once.
 constexpr int kSetChunk = 1024;
+// The extend/prefill kernel holds 256 (its shared memory goes to the K/V ring and the output
+// staging); its sets are chunked the same way.
+constexpr int kAttnSetChunk = 256;
+// Slots of the extend/prefill kernel's work-item counters (attn_tc.cu): launch k uses slot
+// k % kAttnSchedSlots.
+constexpr int kAttnSchedSlots = 64;
 
 struct DecodeParams {
   unsigned int* err;  // device error word
@@ -65,7 +71,7 @@ struct AttnParams {
   int32_t cls;
   int32_t max_reqs;
   int32_t batch_reqs;
-  int32_t set_offset;           // first set position of this launch's chunk (a multiple of kSetChunk)
+  int32_t set_offset;           // first set position of this launch's chunk (a multiple of kAttnSetChunk)
   int32_t Hq, Hkv, G;
   int64_t num_blocks;
   int64_t num_tokens;           // rows of q / k_new / v_new
@@ -74,6 +80,7 @@ struct AttnParams {
   float scale_log2;
   float ctx_scale_log2;  // cached-context key tiles: softmax scale * key scale * log2(e)
   float ctx_v_scale;     // cached-context tiles: P is multiplied by the value scale for P V
+  int32_t sched_slot;    // this launch's work-item counter slot (< kAttnSchedSlots)
 };
 
 // Extend over an FP8 cache: the set's context blocks gathered into a bf16 pool (exact E4M3
@@ -125,6 +132,7 @@ enum AttrSlot {
   kAttrAttn128,
   kAttrAttn64Scaled,
   kAttrAttn128Scaled,
+  kAttrAttn128Fp8,
   kAttrMla,
   kAttrCount
 };
@@ -156,10 +164,13 @@ cudaError_t launch_ctx_dequant(const CtxDequantParams& p, cudaStream_t stream);
 cudaError_t launch_mla_decode(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, int* launches);
 size_t mla_workspace_bytes(int Hq);
 size_t mla_workspace_ctr_offset(int Hq);
+// Cached context of the extend kernel: a bf16 cache, a bf16 pool of an FP8 cache's E4M3 values,
+// or the FP8 cache's codes (head_dim 128), converted in the kernel.
+constexpr int kAttnCtxBf16 = 0, kAttnCtxPool = 1, kAttnCtxFp8 = 2;
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
 // (ignored for prefill).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const CUtensorMap& tm_ck,
-                             const CUtensorMap& tm_cv, int D, cudaStream_t stream, int* launches);
+                             const CUtensorMap& tm_cv, int D, int ctx_kind, cudaStream_t stream, int* launches);
 
 }  // namespace pkv

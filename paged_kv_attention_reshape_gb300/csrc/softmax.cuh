@@ -41,5 +41,14 @@ __device__ __forceinline__ uint32_t bf16x2(uint64_t v) {
   return r;
 }
 
+// fp16 pair {lo, hi} (round to nearest even) from an fp32 pair
+__device__ __forceinline__ uint32_t f16x2(uint64_t v) {
+  float lo, hi;
+  unf2(v, lo, hi);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 }  // namespace sm
 }  // namespace pkv

@@ -356,6 +356,29 @@ def test_extend_fp8_request_set_and_peaked(pkv):
     assert _errors(pkv) == 0
 
 
+@pytest.mark.parametrize("G", [2, 8, 16])
+def test_extend_fp8_codes_converted_in_the_kernel(pkv, G):
+    """head_dim 128 over an E4M3 cache: the kernel loads the context's codes and converts them
+    in shared memory (no workspace). Contexts of many tiles with ragged ends, new tokens over
+    several tiles, a small value scale (new values stored divided by it), peaked queries."""
+    Hkv = 2
+    new = [300, 129, 1, 128]
+    ctx = [5000, 2047, 700, 0]
+    b = gen.extend_batch(new, ctx, Hq=G * Hkv, Hkv=Hkv, D=128, seed=700 + G, q_scale=2.0)
+    ks, vs = gen.fp8_scale(0.5), gen.fp8_scale(0.2)
+    kc, vc = gen.fp8_codes(b.k_cache * 0.1, ks), gen.fp8_codes(b.v_cache * 0.05, vs)
+    assert pkv.extend_fp8_workspace_size(b.R, b.R, max(b.seq_lens_list), b.block_tables.shape[1], Hkv, 128) == 0
+    g = b.to(DEV)
+    scale = default_scale(128)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((b.T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kc.to(DEV), vc.to(DEV), g.block_tables,
+                    max(new), max(b.seq_lens_list), scale=scale, k_scale=ks, v_scale=vs, out=out, lse=lse)
+    ref, ref_lse = _fp8_extend_ref(b, kc.numpy(), vc.numpy(), ks, vs, scale)
+    compare_attention(out, lse, ref, ref_lse, what=f"extend fp8 in-kernel G={G}")
+    assert _errors(pkv) == 0
+
+
 # ---- randomized shapes -------------------------------------------------------------------------
 
 @pytest.mark.parametrize("seed", range(12))

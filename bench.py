@@ -598,7 +598,8 @@ def bench_mixed(pkv, dev, stream, timer, steps, warmup):
 
 def bench_mixed_fp8(pkv, dev, stream, timer, steps, warmup):
     """The mixed step over an FP8 (E4M3) cache: quantising write, decode dequantising as it
-    reads, extend through the gather of its context into a bf16 workspace, prefill (no cache)."""
+    reads, extend converting the context's codes in the kernel (head_dim 128: no workspace),
+    prefill (no cache)."""
     b = mixed_workload(dev)
     R, T = b.R, b.T
     ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
@@ -849,8 +850,8 @@ def profile_case(pkv, args):
                                      b.block_tables, 512, max(b.seq_lens_list))
         what = "extend 2 x (16000 cached + 512 new)"
     elif args.profile == "extend_fp8":
-        # the extend case over an FP8 (E4M3) cache: the context gather (~530 MB of codes read
-        # and bf16 written per launch), then the scaled tensor-core kernel
+        # the extend case over an FP8 (E4M3) cache: the tensor-core kernel reads the context's
+        # codes (~131 MB a launch over both K and V) and converts them in shared memory
         b = gen.extend_batch([512, 512], [16000, 16000], Hq=64, Hkv=8, D=128, seed=3, device=dev)
         ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
         kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)

@@ -14,11 +14,14 @@
 // The online softmax keeps a running (max, sum) per row; rescaling O by exp(m_old - m_new) is
 // the LSE merge of each 128-key partial into the result so far.
 //
-// Roles (320 threads, up to 200 registers each):
-//   warps 0-3  softmax of head slot 0 (thread t owns query row t = TMEM lane t)
+// Roles (320 threads at 168 registers; 384 for an FP8 context):
+//   warps 0-3  softmax of head slot 0 (thread t owns query row t = TMEM lane t), then the
+//              slot's epilogue (O out of TMEM, normalised, stored through a staging tile)
 //   warps 4-7  softmax of head slot 1
-//   warp 8     TMA producer: Q tiles, then K and V tiles into a ring of NBUF tile buffers
+//   warp 8     TMA producer: takes the CTA's next work item and publishes it to the other
+//              roles, then loads its Q tiles and K and V tiles into a ring of NBUF tile buffers
 //   warp 9     MMA issuer (one thread): S_i = Q_i K^T (SS), O_i += P_i V (P read from TMEM)
+//   warps 10-11 (FP8 context only) convert E4M3 code tiles, Q and new-token tiles to fp16
 // Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1; P_i (bf16 pairs) overwrites the first
 // half of S_i, which the next S_i = Q_i K^T only writes after the P_i V product that reads it
 // (tcgen05 MMAs issued by one thread run in order).

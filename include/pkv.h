@@ -12,8 +12,12 @@
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except where a
  *     comment says "host". The library allocates no device memory and keeps no state
- *     between calls other than one per-device error word (pkv_device_errors) and the
- *     handoff handles the caller creates (pkv_handoff_create).
+ *     between calls other than one per-device error word (pkv_device_errors), the handoff
+ *     handles the caller creates (pkv_handoff_create) and, per device, 64 work-item counter
+ *     slots of the extend/prefill kernel (each launch takes the next slot and leaves it at zero;
+ *     a launch shares its slot only with the launch 64 extend/prefill launches later, so at
+ *     most 63 other such launches may be in flight at once on one device, and one captured
+ *     graph must not be replayed on two streams at the same time).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and returns after checking its host-side arguments and enqueueing its kernels. It
  *     never synchronises, except pkv_device_errors.

@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
   long long* s_item = reinterpret_cast<long long*>(smem + C::ITEM_OFF);
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_claim;  // 1: items are claimed from the launch's counter; 0: static snake deal
   __shared__ int s_scan[12];
 
   pdl_wait();
@@ -394,10 +395,28 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     __syncthreads();
   }
   if (tid == 0) s_start[n] = carry;
+  __syncthreads();
+  if (warp == 0) {
+    // the average cost of the launch's items (key tiles) decides how they are dealt: a
+    // request with nct context tiles and nt q-tiles has items of nct + 1 .. nct + nt tiles
+    long long tiles = 0, qtiles = 0;
+    for (int i = lane; i < n; i += 32) {
+      const long long nt = s_start[i + 1] - s_start[i], nct = (s_req[s_perm[i]].w + 127) / 128;
+      tiles += nt * nct + nt * (nt + 1) / 2;
+      qtiles += nt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+      qtiles += __shfl_xor_sync(0xffffffffu, qtiles, o);
+    }
+    if (lane == 0) s_claim = tiles < static_cast<long long>(kDynamicBelow) * qtiles ? 1 : 0;
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+  const bool claim = s_claim != 0;
   const int HP = p.G >= 2 ? p.Hq / 2 : p.Hq;
   const int64_t W = static_cast<int64_t>(carry) * HP;
   if constexpr (C::ONE_READ) {
@@ -416,8 +435,16 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t sc = 0, oc = 0;
     const float lvs = SCALED ? log2f(p.ctx_v_scale) : 0.f;  // new-token tiles' extra shift
+    int64_t w_static = blockIdx.x;
+    int odd = 0;
     for (uint32_t k = 0;; ++k) {
-      const long long w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, k, &s_abort, p.err, lane);
+      long long w;
+      if (claim) {
+        w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, k, &s_abort, p.err, lane);
+      } else {
+        w = w_static < W ? w_static : -1;
+        w_static = tc_next(w_static, odd);
+      }
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (slot >= it.nslot) continue;
@@ -666,42 +693,29 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     }
     uint32_t kvc = 0;
     bool ok = true;
-    // the average cost of the launch's items (key tiles) decides how they are dealt: a
-    // request with nct context tiles and nt q-tiles has items of nct + 1 .. nct + nt tiles
-    long long tiles = 0, qtiles = 0;
-    for (int i = lane; i < n; i += 32) {
-      const long long nt = s_start[i + 1] - s_start[i], nct = (s_req[s_perm[i]].w + 127) / 128;
-      tiles += nt * nct + nt * (nt + 1) / 2;
-      qtiles += nt;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
-      qtiles += __shfl_xor_sync(0xffffffffu, qtiles, o);
-    }
-    const bool claim = tiles < static_cast<long long>(kDynamicBelow) * qtiles;
     int64_t w_static = blockIdx.x;
     int odd = 0;
     for (uint32_t items = 0; ok; ++items) {
       // the Q buffer is free (the previous item's S products are done): take the next item and
       // publish it to the MMA and softmax warps
       if (items > 0 && !tc_wait_warp(q_empty, (items - 1) & 1, &s_abort, p.err)) break;
-      const int e = static_cast<int>(items % C::ITEM_RING);
-      if (items >= C::ITEM_RING && !tc_wait_warp(&item_empty[e], (items / C::ITEM_RING - 1) & 1, &s_abort, p.err))
-        break;
-      long long w = 0;
-      if (lane == 0) {
-        if (claim) {
+      long long w;
+      if (claim) {
+        const int e = static_cast<int>(items % C::ITEM_RING);
+        if (items >= C::ITEM_RING && !tc_wait_warp(&item_empty[e], (items / C::ITEM_RING - 1) & 1, &s_abort, p.err))
+          break;
+        w = 0;
+        if (lane == 0) {
           w = static_cast<long long>(atomicAdd(&g_attn_next[p.sched_slot], 1u));
-        } else {
-          w = w_static;
-          w_static = tc_next(w_static, odd);
+          if (w >= W) w = -1;
+          *reinterpret_cast<volatile long long*>(&s_item[e]) = w;
+          mbar_arrive(&item_full[e]);
         }
-        if (w >= W) w = -1;
-        *reinterpret_cast<volatile long long*>(&s_item[e]) = w;
-        mbar_arrive(&item_full[e]);
+        w = __shfl_sync(0xffffffffu, w, 0);
+      } else {
+        w = w_static < W ? w_static : -1;
+        w_static = tc_next(w_static, odd);
       }
-      w = __shfl_sync(0xffffffffu, w, 0);
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (lane == 0) {
@@ -777,8 +791,16 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
         tc::mma_ts(tmem + ocol(slot), tmem + scol(slot) + k * 8,
                    tc::smem_desc(vb + k * 2048, C::HALF_BYTES, 1024), C::IDESC_PV, (acc || k > 0) ? 1u : 0u);
     };
+    int64_t w_static = blockIdx.x;
+    int odd = 0;
     for (; ok; ++items) {
-      const long long w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, items, &s_abort, p.err, lane);
+      long long w;
+      if (claim) {
+        w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, items, &s_abort, p.err, lane);
+      } else {
+        w = w_static < W ? w_static : -1;
+        w_static = tc_next(w_static, odd);
+      }
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       const bool two = it.nslot == 2;
@@ -862,8 +884,16 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     const uint32_t q_base = smem_u32(sQ), ring_base = smem_u32(ring);
     uint32_t kvc = 0;
     bool ok = true;
+    int64_t w_static = blockIdx.x;
+    int odd = 0;
     for (uint32_t k = 0; ok; ++k) {
-      const long long w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, k, &s_abort, p.err, lane);
+      long long w;
+      if (claim) {
+        w = tc_take_item<C::ITEM_RING>(s_item, item_full, item_empty, k, &s_abort, p.err, lane);
+      } else {
+        w = w_static < W ? w_static : -1;
+        w_static = tc_next(w_static, odd);
+      }
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (!tc_wait_warp(q_full, k & 1, &s_abort, p.err)) break;

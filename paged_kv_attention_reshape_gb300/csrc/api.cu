@@ -592,7 +592,7 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
   if (reqs.max_reqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
-  if (num_tokens > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens > INT32_MAX || num_tokens * Hq > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   if (q == nullptr || k == nullptr || v == nullptr || cu_q == nullptr || out == nullptr)
     return PKV_ERR_INVALID_ARG;
   if (cache != nullptr && (seq_lens == nullptr || block_tables == nullptr || max_blocks <= 0))
@@ -622,11 +622,11 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   p.scale_log2 = scale * 1.4426950408889634f;
   p.ctx_scale_log2 = scale * ctx_k_scale * 1.4426950408889634f;
   p.ctx_v_scale = ctx_v_scale;
-  CUtensorMap tq, tk, tv, tck, tcv;
+  CUtensorMap tq, tk, tv, tck, tcv, tqf;
   std::memset(&tck, 0, sizeof tck);
   std::memset(&tcv, 0, sizeof tcv);
   if (!encode_rows(&tq, q, num_tokens, Hq, D, 128) || !encode_rows(&tk, k, num_tokens, Hkv, D, 128) ||
-      !encode_rows(&tv, v, num_tokens, Hkv, D, 128))
+      !encode_rows(&tv, v, num_tokens, Hkv, D, 128) || !encode_rows(&tqf, q, num_tokens * Hq, 1, D, 128))
     return PKV_ERR_CUDA;
   if (cache != nullptr &&
       (!encode_cache(&tck, cache->k, *cache) || !encode_cache(&tcv, cache->v, *cache)))
@@ -635,7 +635,7 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
   for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kAttnSetChunk) {
     p.set_offset = off;
     p.sched_slot = next_sched_slot();
-    st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, D, cache != nullptr ? ctx_kind : kAttnCtxBf16,
+    st = cuda_status(launch_attention(p, tq, tk, tv, tck, tcv, tqf, D, cache != nullptr ? ctx_kind : kAttnCtxBf16,
                                       reinterpret_cast<cudaStream_t>(stream), &launches));
   }
   t_launches += launches;

@@ -89,10 +89,20 @@ struct TcCfg {
 __device__ __forceinline__ constexpr uint32_t scol(int slot) { return slot * 128u; }
 __device__ __forceinline__ constexpr uint32_t ocol(int slot) { return 256u + slot * 128u; }
 
+// A work item: a 128-row query tile of a request for a pair of query heads of one KV head (two
+// slots), or, for a one-token request (a decode) when G >= 2, the request's token for all G
+// query heads of one KV head, the heads on the tile's rows (dec; one slot, rows 0 .. G-1), so
+// that the KV head's context is read once for the G heads.
 struct TcItem {
-  int r, q_len, C, qr0, nrows, nct, NT, h0, nslot, kh;
+  int r, q_len, C, qr0, nrows, nct, NT, h0, nslot, kh, dec;
   int64_t row0;
 };
+
+// Items of a set request: Hkv for a packed decode, (q-tiles) x HP otherwise.
+__device__ __forceinline__ bool tc_dec(const int4& q, int G) { return q.z == 1 && G >= 2; }
+__device__ __forceinline__ int tc_items(const int4& q, int G, int Hkv, int HP) {
+  return tc_dec(q, G) ? Hkv : (q.z + 127) / 128 * HP;
+}
 
 // This launch's chunk of the request set: positions [begin, begin + n), the set's positions
 // set_offset .. set_offset + kAttnSetChunk - 1 that exist.
@@ -112,26 +122,39 @@ __device__ __forceinline__ void tc_resolve_set(const AttnParams& p, int& begin, 
 
 // Work item w (all roles walk the same sequence of items); s_req holds {request id, first
 // query row, q_len, cached tokens} of each request of the set, s_perm the set positions by
-// decreasing tile cost, s_start the prefix of q-tiles in that order.
+// decreasing tile cost, s_start the prefix of items in that order.
 __device__ __forceinline__ TcItem tc_item(const AttnParams& p, const int* s_start, const int4* s_req,
                                           const int* s_perm, int n, int64_t w, int HP) {
   TcItem it;
-  const int tg = static_cast<int>(w / HP), hp = static_cast<int>(w % HP);
+  const int wi = static_cast<int>(w);
   int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_start[mid] <= tg) lo = mid; else hi = mid - 1;
+    if (s_start[mid] <= wi) lo = mid; else hi = mid - 1;
   }
   const int4 q = s_req[s_perm[lo]];
+  const int idx = wi - s_start[lo];
   it.r = q.x;
   it.row0 = q.y;
   it.q_len = q.z;
   it.C = q.w;
-  const int ntile = s_start[lo + 1] - s_start[lo];
-  const int ti = ntile - 1 - (tg - s_start[lo]);  // later (heavier) tiles of a request first
+  it.nct = (it.C + 127) / 128;
+  if (tc_dec(q, p.G)) {
+    it.dec = 1;
+    it.qr0 = 0;
+    it.nrows = p.G;  // rows = the KV head's query heads
+    it.NT = it.nct + 1;
+    it.nslot = 1;
+    it.kh = idx;
+    it.h0 = idx * p.G;
+    return it;
+  }
+  it.dec = 0;
+  const int ntile = (q.z + 127) / 128;
+  const int ti = ntile - 1 - idx / HP;  // later (heavier) tiles of a request first
+  const int hp = idx % HP;
   it.qr0 = ti * 128;
   it.nrows = min(128, it.q_len - it.qr0);
-  it.nct = (it.C + 127) / 128;
   it.NT = it.nct + ti + 1;
   it.nslot = p.G >= 2 ? 2 : 1;
   it.h0 = p.G >= 2 ? 2 * hp : hp;
@@ -278,7 +301,8 @@ template <int D, int KIND>
 __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kernel(
     const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __grid_constant__ CUtensorMap tm_ck, const __grid_constant__ CUtensorMap tm_cv) {
+    const __grid_constant__ CUtensorMap tm_ck, const __grid_constant__ CUtensorMap tm_cv,
+    const __grid_constant__ CUtensorMap tm_qf) {
   using C = TcCfg<D, KIND>;
   constexpr bool SCALED = KIND != kCtxBf16;
   extern __shared__ uint8_t smem_raw[];
@@ -372,11 +396,12 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     s_perm[rank] = i;
   }
   __syncthreads();
-  // exclusive prefix of 128-row q-tiles in that order
+  // exclusive prefix of the requests' items in that order
+  const int HP = p.G >= 2 ? p.Hq / 2 : p.Hq;
   int carry = 0;
   for (int base = 0; base < n; base += C::THREADS) {
     const int j = base + tid;
-    const int t = j < n ? (s_req[s_perm[j]].z + 127) / 128 : 0;
+    const int t = j < n ? tc_items(s_req[s_perm[j]], p.G, p.Hkv, HP) : 0;
     int x = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -399,11 +424,18 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
   if (warp == 0) {
     // the average cost of the launch's items (key tiles) decides how they are dealt: a
     // request with nct context tiles and nt q-tiles has items of nct + 1 .. nct + nt tiles
+    // (HP of each), a packed decode Hkv items of nct + 1
     long long tiles = 0, qtiles = 0;
     for (int i = lane; i < n; i += 32) {
-      const long long nt = s_start[i + 1] - s_start[i], nct = (s_req[s_perm[i]].w + 127) / 128;
-      tiles += nt * nct + nt * (nt + 1) / 2;
-      qtiles += nt;
+      const int4 q = s_req[s_perm[i]];
+      const long long ni = s_start[i + 1] - s_start[i], nct = (q.w + 127) / 128;
+      if (tc_dec(q, p.G)) {
+        tiles += ni * (nct + 1);
+      } else {
+        const long long nt = ni / HP;
+        tiles += HP * (nt * nct + nt * (nt + 1) / 2);
+      }
+      qtiles += ni;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -417,8 +449,7 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
   const bool claim = s_claim != 0;
-  const int HP = p.G >= 2 ? p.Hq / 2 : p.Hq;
-  const int64_t W = static_cast<int64_t>(carry) * HP;
+  const int64_t W = carry;
   if constexpr (C::ONE_READ) {
     static_assert(C::THREADS == 384 && 2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_OTHER == C::THREADS * 168,
                   "register split");
@@ -448,7 +479,9 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (slot >= it.nslot) continue;
-      const int qi = it.qr0 + t;  // query index of this row within its request
+      // query index of this row within its request (a packed decode's rows are heads of its one
+      // token)
+      const int qi = it.dec ? 0 : it.qr0 + t;
       float m = -CUDART_INF_F, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.NT && ok; ++j) {
@@ -636,9 +669,12 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
       if (!tc_wait_warp(&o_final[slot], oc & 1, &s_abort, p.err)) break;
       ++oc;
       tc::fence_after_sync();
-      const int h = it.h0 + slot;
       const int64_t row = it.row0 + qi;
       const bool write = t < it.nrows && row < p.num_tokens;
+      // out and lse of tile row tr sit at flat row orow0 + tr * ostep of [T * Hq] (head h0 + slot
+      // of token row0 + qr0 + tr; for a packed decode head h0 + tr of token row0)
+      const int64_t orow0 = it.dec ? it.row0 * p.Hq + it.h0 : (row - t) * p.Hq + it.h0 + slot;
+      const int ostep = it.dec ? 1 : p.Hq;
       const float inv = l > 0.f ? (SCALED ? p.ctx_v_scale : 1.f) / l : 0.f;
       // O leaves through the warp's staging tile (32 rows x 32 columns at a time): each thread
       // puts its row there, then every store instruction writes 8 rows x 64 contiguous bytes
@@ -670,20 +706,21 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
           const int rr = i * 8 + (lane >> 2), kk = lane & 3;  // row of the warp's 32, 16-byte chunk
           const uint4 v = ld_shared_v4(stg + rr * 64 + ((kk ^ ((rr >> 1) & 3)) << 4));
           const int tr = wrow0 + rr;
-          const int64_t grow = row + (tr - t);
-          if (tr < it.nrows && grow < p.num_tokens)
-            *reinterpret_cast<uint4*>(p.out + (grow * p.Hq + h) * D + c * 32 + kk * 8) = v;
+          const int64_t tok = it.dec ? it.row0 : row + (tr - t);
+          if (tr < it.nrows && tok < p.num_tokens)
+            *reinterpret_cast<uint4*>(p.out + (orow0 + static_cast<int64_t>(tr) * ostep) * D + c * 32 + kk * 8) = v;
         }
         __syncwarp();
       }
       if (write && p.lse)
-        p.lse[row * p.Hq + h] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        p.lse[orow0 + static_cast<int64_t>(t) * ostep] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       tc::fence_before_sync();
     }
   } else if (warp == 8) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_qf);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       if (p.seq_lens != nullptr) {
@@ -720,11 +757,20 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, it.nslot * C::TILE_BYTES);
-        for (int sl = 0; sl < it.nslot; ++sl)
+        if (it.dec) {
+          // the token's heads h0 .. h0 + G - 1 as the tile's rows: 128 rows of q viewed as
+          // [T * Hq][D] from row row0 * Hq + h0 (rows past G are other heads, never written)
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf)
-            tma_load_3d(sQ + sl * C::TILE_BYTES + hf * C::HALF_BYTES, &tm_q, q_full, 0,
-                        (it.h0 + sl) * C::HALVES + hf, static_cast<int>(it.row0) + it.qr0);
+            tma_load_3d(sQ + hf * C::HALF_BYTES, &tm_qf, q_full, 0, hf,
+                        static_cast<int>(it.row0 * p.Hq + it.h0));
+        } else {
+          for (int sl = 0; sl < it.nslot; ++sl)
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              tma_load_3d(sQ + sl * C::TILE_BYTES + hf * C::HALF_BYTES, &tm_q, q_full, 0,
+                          (it.h0 + sl) * C::HALVES + hf, static_cast<int>(it.row0) + it.qr0);
+        }
       }
       const int32_t* table = p.block_tables ? p.block_tables + static_cast<int64_t>(it.r) * p.max_blocks : nullptr;
       const int ctx_blocks = (it.C + 15) / 16;
@@ -773,7 +819,8 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     }
   } else if (warp == 9) {
     // ======================= MMA issuer =======================
-    uint32_t kvc = 0, items = 0, pc = 0;
+    // P tiles consumed per slot (their own counts: a packed decode item uses slot 0 only)
+    uint32_t kvc = 0, items = 0, pc = 0, pc1 = 0;
     bool ok = true;
     auto qk = [&](int slot, const uint8_t* kbuf) {
       const uint32_t qa = smem_u32(sQ + slot * C::TILE_BYTES), kb = smem_u32(kbuf);
@@ -818,7 +865,8 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
         }
         __syncwarp();
         if (two && j > 0) {  // O_1 += P_1(j-1) V(j-1)
-          if (!tc_wait_warp(&p_full[1], (pc - 1) & 1, &s_abort, p.err)) { ok = false; break; }
+          if (!tc_wait_warp(&p_full[1], pc1 & 1, &s_abort, p.err)) { ok = false; break; }
+          ++pc1;
           tc::fence_after_sync();
           if (lane == 0) {
             pv(1, ring + prev_vbuf * C::TILE_BYTES, j - 1 > 0);
@@ -865,7 +913,8 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
       }
       if (!ok) break;
       if (two) {
-        if (!tc_wait_warp(&p_full[1], (pc - 1) & 1, &s_abort, p.err)) break;
+        if (!tc_wait_warp(&p_full[1], pc1 & 1, &s_abort, p.err)) break;
+        ++pc1;
         tc::fence_after_sync();
         if (lane == 0) pv(1, ring + prev_vbuf * C::TILE_BYTES, it.NT - 1 > 0);
       }
@@ -950,7 +999,7 @@ template <int D, int KIND>
 static cudaError_t launch_attention_tc_impl(const AttnParams& p, const CUtensorMap& tq,
                                             const CUtensorMap& tk, const CUtensorMap& tv,
                                             const CUtensorMap& tck, const CUtensorMap& tcv,
-                                            cudaStream_t stream, int* launches) {
+                                            const CUtensorMap& tqf, cudaStream_t stream, int* launches) {
   using C = TcCfg<D, KIND>;
   const int slot = KIND == kCtxFp8 ? kAttrAttn128Fp8
                                    : (KIND == kCtxPool ? (D == 64 ? kAttrAttn64Scaled : kAttrAttn128Scaled)
@@ -958,22 +1007,23 @@ static cudaError_t launch_attention_tc_impl(const AttnParams& p, const CUtensorM
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(&attention_tc_kernel<D, KIND>), C::SMEM, slot);
   if (e != cudaSuccess) return e;
   e = launch_pdl(attention_tc_kernel<D, KIND>, dim3(num_sms()), dim3(C::THREADS), C::SMEM, stream, p, tq, tk, tv,
-                 tck, tcv);
+                 tck, tcv, tqf);
   *launches += 1;
   return e;
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const CUtensorMap& tm_ck,
-                             const CUtensorMap& tm_cv, int D, int ctx_kind, cudaStream_t stream, int* launches) {
+                             const CUtensorMap& tm_cv, const CUtensorMap& tm_qf, int D, int ctx_kind,
+                             cudaStream_t stream, int* launches) {
   if (ctx_kind == kAttnCtxFp8) {
     if (D != 128) return cudaErrorInvalidValue;
-    return launch_attention_tc_impl<128, kCtxFp8>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
+    return launch_attention_tc_impl<128, kCtxFp8>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, tm_qf, stream, launches);
   }
   if (ctx_kind == kAttnCtxPool)
-    return D == 64 ? launch_attention_tc_impl<64, kCtxPool>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches)
-                   : launch_attention_tc_impl<128, kCtxPool>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
-  return D == 64 ? launch_attention_tc_impl<64, kCtxBf16>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches)
-                 : launch_attention_tc_impl<128, kCtxBf16>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, stream, launches);
+    return D == 64 ? launch_attention_tc_impl<64, kCtxPool>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, tm_qf, stream, launches)
+                   : launch_attention_tc_impl<128, kCtxPool>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, tm_qf, stream, launches);
+  return D == 64 ? launch_attention_tc_impl<64, kCtxBf16>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, tm_qf, stream, launches)
+                 : launch_attention_tc_impl<128, kCtxBf16>(p, tm_q, tm_k, tm_v, tm_ck, tm_cv, tm_qf, stream, launches);
 }
 }  // namespace pkv

@@ -168,9 +168,10 @@ size_t mla_workspace_ctr_offset(int Hq);
 // or the FP8 cache's codes (head_dim 128), converted in the kernel.
 constexpr int kAttnCtxBf16 = 0, kAttnCtxPool = 1, kAttnCtxFp8 = 2;
 // tm_q over q, tm_k/tm_v over the packed new keys/values, tm_ck/tm_cv over the paged cache
-// (ignored for prefill).
+// (ignored for prefill), tm_qf over q viewed as [T * Hq][D] (one-token requests' heads as rows).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                              const CUtensorMap& tm_v, const CUtensorMap& tm_ck,
-                             const CUtensorMap& tm_cv, int D, int ctx_kind, cudaStream_t stream, int* launches);
+                             const CUtensorMap& tm_cv, const CUtensorMap& tm_qf, int D, int ctx_kind,
+                             cudaStream_t stream, int* launches);
 
 }  // namespace pkv

@@ -827,6 +827,49 @@ def test_mixed_batch_unified_single_call(pkv, D):
     compare_attention(out, lse, ref, ref_lse, rows=np.ones(T, bool), what=f"unified D={D}")
 
 
+@pytest.mark.parametrize("G,Hkv,D,fp8", [(2, 4, 128, False), (4, 2, 64, False), (8, 2, 128, False),
+                                          (16, 1, 64, False), (8, 3, 128, True), (1, 4, 128, False)])
+def test_extend_one_token_requests_pack_heads(pkv, G, Hkv, D, fp8):
+    """One-token requests inside extend_attn (decodes sent through the extend call): their G query
+    heads share one tile (one item per KV head), beside ordinary extend requests in the same
+    launch. Ragged and empty contexts, non-finite values past each context's end."""
+    ctx = [0, 1, 15, 16, 17, 300, 1000, 4095]
+    new = [1] * len(ctx) + [70, 129]
+    ctx = ctx + [50, 200]
+    b = gen.extend_batch(new, ctx, Hq=G * Hkv, Hkv=Hkv, D=D, seed=900 + G * 10 + D + fp8)
+    bt = b.block_tables.numpy()
+    g = b.to(DEV)
+    scale = default_scale(D)
+    kw = {}
+    if fp8:
+        ks, vs = gen.fp8_scale(4.0), gen.fp8_scale(4.5)
+        kc, vc = gen.fp8_codes(b.k_cache, ks), gen.fp8_codes(b.v_cache, vs)
+        for r, C in enumerate(ctx):
+            if C % 16:
+                kc[bt[r, C // 16], C % 16:] = 0x7F
+                vc[bt[r, C // 16], C % 16:] = 0xFF
+        kw = dict(k_scale=ks, v_scale=vs)
+        kcd, vcd = kc.to(DEV), vc.to(DEV)
+    else:
+        kc, vc = b.k_cache.clone(), b.v_cache.clone()
+        for r, C in enumerate(ctx):
+            if C % 16:
+                kc[bt[r, C // 16], C % 16:] = float("nan")
+                vc[bt[r, C // 16], C % 16:] = float("inf")
+        kcd, vcd = kc.to(DEV), vc.to(DEV)
+    out = torch.full_like(g.q, float("nan"))
+    lse = torch.full((b.T, b.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kcd, vcd, g.block_tables, max(new),
+                    max(b.seq_lens_list), scale=scale, out=out, lse=lse, **kw)
+    if fp8:
+        ref, ref_lse = _fp8_extend_ref(b, kc.numpy(), vc.numpy(), ks, vs, scale)
+    else:
+        ref, ref_lse = oracle_extend(b, bits(kc), bits(vc), scale)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, rows=np.ones(b.T, bool), what=f"extend one-token G={G} D={D} fp8={fp8}")
+    assert _errors(pkv) == 0
+
+
 def test_request_set_cut_to_max_reqs_is_flagged(pkv):
     b = gen.decode_batch(6, 10, 60, Hq=4, Hkv=1, D=64, seed=2)
     g = b.to(DEV)

@@ -353,11 +353,15 @@ def bench_decode_fp8(pkv, dev, stream, timer, steps, warmup):
     return dict(step_ms=step_ms, launch_ms=dec_ms, kv_bytes=kv_bytes, alg_bytes=kv_bytes + other, R=R)
 
 
-def bench_mla(pkv, dev, stream, timer, steps, warmup):
+def bench_mla(pkv, dev, stream, timer, steps, warmup, Hq=None):
     """Absorbed MLA decode, DeepSeek-R1-like layer under tensor parallelism 8 (16 query heads
-    over a 576-wide latent, 128 requests at 10K-11K tokens). Step = kv_cache_write of the new
-    tokens' latent rows + mla_decode_attn."""
-    b = gen.mla_batch(**gen.MLA_DEEPSEEK_TP8, device=dev)
+    over a 576-wide latent, 128 requests at 10K-11K tokens); Hq = 128 gives the same layer on one
+    GPU without tensor parallelism. Step = kv_cache_write of the new tokens' latent rows +
+    mla_decode_attn."""
+    cfg = dict(gen.MLA_DEEPSEEK_TP8)
+    if Hq is not None:
+        cfg["Hq"] = Hq
+    b = gen.mla_batch(**cfg, device=dev)
     R, maxs = b.R, max(b.seq_lens_list)
     bt64 = b.block_tables.to(torch.int64)
     pos = (b.seq_lens.to(torch.int64) - 1)
@@ -1041,6 +1045,18 @@ def main():
             summary.update(mla_decode_frac=_r(fr))
         except Exception as e:
             extras["mla_decode"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            # the same layer with all 128 heads on one GPU: compute-bound on the warp-level MMA
+            # (informational; eight groups of 16 heads, L2 serving the groups' repeated reads)
+            r = bench_mla(pkv, dev, stream, timer, max(3, steps // 2), warmup, Hq=128)
+            extras["mla_decode_128"] = {
+                "launch_ms": r["launch_ms"], "latent_gbs": r["lat_bytes"] / (r["launch_ms"] * 1e-3) / 1e9,
+                "mma_tflops": r["flops"] / (r["launch_ms"] * 1e-3) / 1e12,
+                "decode_tokens_per_s": r["R"] / (r["step_ms"] * 1e-3), "device_errors": r["errors"]}
+            summary["mla128_latent_gbs"] = _r(extras["mla_decode_128"]["latent_gbs"])
+        except Exception as e:
+            extras["mla_decode_128"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         for kind in ("prefill", "extend_long"):
             try:

@@ -844,6 +844,14 @@ def profile_case(pkv, args):
         fn = lambda: pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, maxs, gen.MLA_SCALE,
                                          workspace=ws)
         what = f"mla B=32 latent_bytes={sum(b.seq_lens_list) * 1152}"
+    elif args.profile == "mla128":
+        # the same 32 requests with all 128 query heads (the tensor-core kernel on clusters of two)
+        b = gen.mla_batch(32, 10000, 11000, Hq=128, seed=5, device=dev)
+        maxs = max(b.seq_lens_list)
+        ws = torch.empty(max(16, pkv.mla_decode_workspace_size(b.R, 128, maxs)), dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, maxs, gen.MLA_SCALE,
+                                         workspace=ws)
+        what = f"mla 128 heads B=32 latent_bytes={sum(b.seq_lens_list) * 1152}"
     elif args.profile == "prefill":
         b = gen.prefill_batch([4096, 4096], Hq=64, Hkv=8, D=128, seed=5, device=dev)
         fn = lambda: pkv.varlen_prefill_attn(b.q, b.k_new, b.v_new, b.cu_q, 4096)
@@ -885,7 +893,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mla", "prefill", "extend", "extend_fp8", "write_pack"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mla", "mla128", "prefill", "extend", "extend_fp8", "write_pack"], default=None,
                     help="run a reduced case of one kernel --steps times for an ncu capture; prints "
                          "a one-line summary, no benchmark line")
     args = ap.parse_args()

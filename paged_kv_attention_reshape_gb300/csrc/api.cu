@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "mla_tc.h"
 
 namespace pkv {
 
@@ -505,7 +506,7 @@ size_t pkv_mla_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int3
   (void)max_reqs;
   (void)max_seq_len;
   if (num_q_heads <= 0 || num_q_heads % 16 != 0 || num_q_heads > 128) return 0;
-  return mla_workspace_bytes(num_q_heads);
+  return num_q_heads == 128 ? mla_tc_workspace_bytes() : mla_workspace_bytes(num_q_heads);
 }
 
 pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,
@@ -552,18 +553,21 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
   p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.v_scale = 1.f;
-  const size_t need = mla_workspace_bytes(num_q_heads);
+  // all 128 heads of a layer: the tcgen05 kernel on clusters of two CTAs; fewer: mma.sync
+  const bool tc = num_q_heads == 128;
+  const size_t need = tc ? mla_tc_workspace_bytes() : mla_workspace_bytes(num_q_heads);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   p.ws_part = static_cast<float*>(workspace);
-  p.ws_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
-                                                   mla_workspace_ctr_offset(num_q_heads));
+  p.ws_ctr = reinterpret_cast<unsigned long long*>(
+      static_cast<char*>(workspace) + (tc ? mla_tc_meta_offset() : mla_workspace_ctr_offset(num_q_heads)));
   CUtensorMap tm;
   if (!encode_cache(&tm, cache.k, cache)) return PKV_ERR_CUDA;
   int launches = 0;
   for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
     p.set_offset = off;
     p.epoch = next_epoch();
-    st = cuda_status(launch_mla_decode(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches));
+    st = cuda_status(tc ? launch_mla_tc(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches)
+                        : launch_mla_decode(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches));
   }
   t_launches += launches;
   return st;

@@ -95,6 +95,23 @@ def test_mla_deepseek_tp8_full(pkv):
     print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="mla deepseek tp8 full"))
 
 
+def test_mla_deepseek_128_heads_full(pkv):
+    """The same latent batch with all 128 query heads of the layer (no tensor parallelism), the
+    tensor-core kernel on clusters of two CTAs: 8 sampled requests against the oracle, every
+    head; the bench times this call as its 128-head line."""
+    b = gen.mla_batch(**{**gen.MLA_DEEPSEEK_TP8, "Hq": 128}, device="cuda")
+    out, lse = pkv.mla_decode_attn(b.q, b.latent, b.block_tables, b.seq_lens, max(b.seq_lens_list),
+                                   gen.MLA_SCALE)
+    torch.cuda.synchronize()
+    assert pkv.device_errors() == 0
+    sample = np.sort(np.random.default_rng(2).choice(b.R, 8, replace=False)).astype(np.int32)
+    ref, ref_lse = oracle.mla_decode(_host(b.q), _host(b.latent), b.block_tables.cpu().numpy(),
+                                     b.seq_lens.cpu().numpy(), gen.MLA_SCALE, gen.MLA_DV, req_ids=sample)
+    rows = np.zeros(b.R, bool)
+    rows[sample] = True
+    print(compare_attention(out, lse, ref, ref_lse, rows=rows, what="mla deepseek 128 heads full"))
+
+
 def test_mixed_llama70b_full(pkv):
     """192 decode + 8 extend (512 over 4k-32k) + 4 prefill (2k-8k), shuffled: the full step;
     sampled rows of every class checked."""

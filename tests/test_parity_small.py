@@ -429,7 +429,7 @@ def test_random_mixed_batches(pkv, seed):
 @pytest.mark.parametrize("seed", range(6))
 def test_random_mla_batches(pkv, seed):
     rng = np.random.default_rng(3000 + seed)
-    Hq = int(rng.choice([16, 32, 64]))
+    Hq = int(rng.choice([16, 32, 64, 128]))
     R = int(rng.integers(1, 40))
     lens = [int(x) for x in rng.integers(0, int(rng.choice([50, 2000, 20000])), size=R)]
     b = gen.mla_batch(R, 0, 0, Hq=Hq, seq_lens=lens, seed=4000 + seed)
@@ -654,14 +654,16 @@ def _to_dev(b):
                            "block_tables": b.block_tables.to(DEV), "seq_lens": b.seq_lens.to(DEV)})
 
 
+@pytest.mark.parametrize("Hq", [16, 128])
 @pytest.mark.parametrize("ctxs", [[1, 16, 17, 31, 32, 33], [0, 5, 0], [4096, 1, 7000, 15], [30000, 20000]])
-def test_mla_decode_edge_lengths_and_cuts(pkv, ctxs):
+def test_mla_decode_edge_lengths_and_cuts(pkv, ctxs, Hq):
     """Partial last blocks, empty contexts (out 0, lse -inf), and a few long sequences that the
-    shares cut into many pieces (merged in several passes)."""
-    b = gen.mla_batch(len(ctxs), 0, 0, Hq=16, seq_lens=ctxs, seed=len(ctxs) + sum(ctxs) % 97)
+    shares cut into many pieces (merged in several passes). At 128 heads the tensor-core kernel
+    runs: tiles of 112 keys, partial tiles at piece ends, the merge of cut sequences."""
+    b = gen.mla_batch(len(ctxs), 0, 0, Hq=Hq, seq_lens=ctxs, seed=len(ctxs) + sum(ctxs) % 97)
     out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
     ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
-    compare_attention(out, lse, ref, ref_lse, what=f"mla {ctxs}")
+    compare_attention(out, lse, ref, ref_lse, what=f"mla {ctxs} Hq={Hq}")
     empty = np.array(ctxs) == 0
     if empty.any():
         assert np.all(out.float().cpu().numpy()[empty] == 0)
@@ -669,24 +671,48 @@ def test_mla_decode_edge_lengths_and_cuts(pkv, ctxs):
     assert _errors(pkv) == 0
 
 
-@pytest.mark.parametrize("ctxs", [[640], [8320], [80000], [3, 41000, 9000]])
-def test_mla_decode_long_sequences_merge_tree(pkv, ctxs):
-    b = gen.mla_batch(len(ctxs), 0, 0, Hq=16, seq_lens=ctxs, seed=sum(ctxs) % 89)
+@pytest.mark.parametrize("ctxs,Hq", [([640], 16), ([8320], 16), ([80000], 16), ([3, 41000, 9000], 16),
+                                     ([640], 128), ([8320], 128), ([3, 41000, 9000], 128)])
+def test_mla_decode_long_sequences_merge_tree(pkv, ctxs, Hq):
+    b = gen.mla_batch(len(ctxs), 0, 0, Hq=Hq, seq_lens=ctxs, seed=sum(ctxs) % 89)
     out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
     ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
-    compare_attention(out, lse, ref, ref_lse, what=f"mla long {ctxs}")
+    compare_attention(out, lse, ref, ref_lse, what=f"mla long {ctxs} Hq={Hq}")
     assert _errors(pkv) == 0
 
 
-def test_mla_decode_peaked_softmax(pkv):
-    b = gen.mla_batch(6, 100, 2000, Hq=16, seed=93, q_scale=3.0)
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_mla_decode_peaked_softmax(pkv, Hq):
+    b = gen.mla_batch(6, 100, 2000, Hq=Hq, seed=93, q_scale=3.0)
     out, lse = _mla(pkv, _to_dev(b), gen.MLA_SCALE)
     ref, ref_lse = _mla_ref(b, gen.MLA_SCALE)
-    compare_attention(out, lse, ref, ref_lse, what="mla peaked")
+    compare_attention(out, lse, ref, ref_lse, what=f"mla peaked Hq={Hq}")
+    assert _errors(pkv) == 0
 
 
-def test_mla_decode_nonfinite_past_the_end_is_ignored(pkv):
-    b = gen.mla_batch(4, 5, 90, Hq=16, seed=94)
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_mla_decode_running_max_grows_late(pkv, Hq):
+    """Each sequence's first 200 latent rows are scaled down 20x, so the scores of its first key
+    tiles are small and the running max grows by far more than the lazy-rescale threshold
+    (8 in log2 units) later on: the kernels must rescale the accumulated output (at 128 heads,
+    CTA 1 of the pair rescales O in tensor memory when CTA 0 reports it)."""
+    b = gen.mla_batch(5, 600, 3000, Hq=Hq, seed=97, q_scale=3.0)
+    lat = b.latent.clone()
+    bt = b.block_tables.numpy()
+    for r, n in enumerate(b.seq_lens_list):
+        for j in range(min(n, 200)):
+            blk, off = bt[r, j // 16], j % 16
+            lat[blk, off] = (lat[blk, off].float() * 0.05).to(torch.bfloat16)
+    out, lse = pkv.mla_decode_attn(b.q.to(DEV), lat.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV),
+                                   max(b.seq_lens_list), gen.MLA_SCALE)
+    ref, ref_lse = _mla_ref(b, gen.MLA_SCALE, latent=lat)
+    compare_attention(out, lse, ref, ref_lse, what=f"mla late max Hq={Hq}")
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_mla_decode_nonfinite_past_the_end_is_ignored(pkv, Hq):
+    b = gen.mla_batch(4, 5, 90, Hq=Hq, seed=94)
     lat = b.latent.clone()
     bt = b.block_tables.numpy()
     for r, n in enumerate(b.seq_lens_list):
@@ -694,20 +720,21 @@ def test_mla_decode_nonfinite_past_the_end_is_ignored(pkv):
     out, lse = pkv.mla_decode_attn(b.q.to(DEV), lat.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV),
                                    max(b.seq_lens_list), gen.MLA_SCALE)
     ref, ref_lse = _mla_ref(b, gen.MLA_SCALE, latent=lat)
-    compare_attention(out, lse, ref, ref_lse, what="mla nan tail")
+    compare_attention(out, lse, ref, ref_lse, what=f"mla nan tail Hq={Hq}")
 
 
-def test_mla_decode_request_set_and_query_rows(pkv):
+@pytest.mark.parametrize("Hq", [16, 128])
+def test_mla_decode_request_set_and_query_rows(pkv, Hq):
     """A request set given by order/bounds (the decode class of a reordered batch) with query
     rows taken through cu_q: only the set's rows are written."""
     R = 9
-    b = gen.mla_batch(R, 1, 900, Hq=16, seed=95)
+    b = gen.mla_batch(R, 1, 900, Hq=Hq, seed=95)
     order = torch.tensor([7, 2, 5, 0, 8, 1, 3, 4, 6], dtype=torch.int32)
     bounds = torch.tensor([2, 7, 9, 9], dtype=torch.int32)  # the set: order[2:7]
     cu_q = torch.tensor([3 * r for r in range(R + 1)], dtype=torch.int32)  # query row of r = 3r
-    q = gen.randn_bf16((3 * R, 16, 576), torch.Generator().manual_seed(6), "cpu")
-    out = torch.full((3 * R, 16, gen.MLA_DV), float("nan"), dtype=torch.bfloat16, device=DEV)
-    lse = torch.full((3 * R, 16), float("nan"), dtype=torch.float32, device=DEV)
+    q = gen.randn_bf16((3 * R, Hq, 576), torch.Generator().manual_seed(6), "cpu")
+    out = torch.full((3 * R, Hq, gen.MLA_DV), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((3 * R, Hq), float("nan"), dtype=torch.float32, device=DEV)
     pkv.mla_decode_attn(q.to(DEV), b.latent.to(DEV), b.block_tables.to(DEV), b.seq_lens.to(DEV),
                         max(b.seq_lens_list), gen.MLA_SCALE, cu_q=cu_q.to(DEV),
                         reqs=pkv.Reqs(5, R, order.to(DEV), bounds.to(DEV), 0), out=out, lse=lse)

@@ -563,7 +563,8 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
   CUtensorMap tm;
   if (!encode_cache(&tm, cache.k, cache)) return PKV_ERR_CUDA;
   int launches = 0;
-  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += kSetChunk) {
+  const int chunk = tc ? kMlaTcSetChunk : kSetChunk;
+  for (int32_t off = 0; off < reqs.max_reqs && st == PKV_OK; off += chunk) {
     p.set_offset = off;
     p.epoch = next_epoch();
     st = cuda_status(tc ? launch_mla_tc(p, tm, reinterpret_cast<cudaStream_t>(stream), &launches)

@@ -24,15 +24,23 @@
 // one share per cluster. A sequence cut at share edges leaves a normalised partial and its LSE
 // per piece in the workspace; a second kernel merges each cut sequence's pieces by their LSEs.
 //
-// Roles (256 threads a CTA):
-//   CTA 0: warp 0 TMA producer (score chunks), warp 1 MMA issuer, warp 2 sends staged P tiles,
-//          warps 4-7 softmax (thread t owns head t = TMEM lane t), also load Q into TMEM.
-//   CTA 1: warp 0 TMA producer (value stages), warp 1 MMA issuer, warps 4-7 correction and
-//          epilogue (thread t owns O row t).
-// Cross-CTA signals: the P slot of tile t in CTA 1 is filled by the bulk copy (complete_tx on
-// CTA 1's p_full) and freed by CTA 1 back to CTA 0's p_free: one arrival from CTA 1's tensor
-// core when the products reading the slot are done (a multicast commit) and one from each
-// correction warp once it has read the slot's rescale factors. Every wait is bounded.
+// Roles (320 threads a CTA):
+//   CTA 0: warps 0-3 TMA producers of the score chunks (warp q loads ring stages 2q, 2q + 1 with
+//          one instruction: a warp's TMA instructions complete one after another, so four warps
+//          and 14 boxes an instruction keep the ring fed), warps 4-7 softmax (thread t owns
+//          head t = TMEM lane t; they also load each piece's Q into TMEM), warp 8 the MMA issuer
+//          (one thread), warp 9 sends the staged P tiles and, at the end, the merge record.
+//   CTA 1: warps 0-3 TMA producers of the value stages (256 dims of a tile each; warp q loads
+//          its 64-dim chunk of every stage), warps 4-7 correction and epilogue (thread t owns
+//          O row t), warp 8 the MMA issuer: O += P V in two N = 256 halves per tile.
+// Cross-CTA signals: the P slot of tile t in CTA 1 (three slots) is filled by the bulk copy
+// (complete_tx on CTA 1's p_full) and freed back to CTA 0's p_free by one arrival from CTA 1's
+// tensor core when the products reading the slot are done (a multicast commit) and one from
+// each correction warp once it has read the slot's rescale factors. Every wait is bounded.
+//
+// What bounds it: each SM's TMA engine moves these 128-byte row segments (a 64-dim chunk of
+// 16 latent rows per box) at about 60 GB/s, and CTA 0 takes in every byte of its share's
+// latent rows (126 KB a tile) plus sends P (33 KB a tile).
 #include <math_constants.h>
 
 #include <mutex>
@@ -54,8 +62,9 @@ struct MtCfg {
   static constexpr int KCH = DK / 64;                  // 9 score chunks of 64 dims
   static constexpr int CH_BYTES = NK * 128;            // one chunk of a tile: 112 rows x 128 B
   static constexpr int NSK = 8;                        // CTA 0 ring: score chunks
-  static constexpr int VST_BYTES = 2 * CH_BYTES;       // CTA 1 stage: 128 value dims of a tile
-  static constexpr int NSV = 4;                        // CTA 1 ring: a whole tile's values
+  static constexpr int VST_BYTES = 4 * CH_BYTES;       // CTA 1 stage: 256 value dims of a tile
+  static constexpr int NSV = 2;                        // CTA 1 ring: a whole tile's values
+  static constexpr int NPROD = 4;                      // producer warps: a warp's TMA issues run one at a time
   static constexpr int RING_BYTES = NSK * CH_BYTES;
   static_assert(RING_BYTES == NSV * VST_BYTES, "the two rings share one region");
   // P tile: [2 chunks of 64 keys][128 rows][128 B], 128-byte swizzle (keys 112..127 unused);
@@ -65,18 +74,20 @@ struct MtCfg {
   static constexpr int TR_ALPHA = P_BYTES, TR_INVL = P_BYTES + 512, TR_FLAGS = P_BYTES + 1024;
   static constexpr int XFER_BYTES = P_BYTES + 1024 + 16;  // what one bulk copy moves
   static constexpr int SLOT_BYTES = 34 * 1024;            // staging buffer / slot stride
+  static constexpr int NSLOT = 3;                        // P staging buffers (CTA 0) and slots (CTA 1)
   static constexpr int XFER_OFF = RING_BYTES;             // CTA 0: staging; CTA 1: P slots
-  static constexpr int MAXR = kSetChunk;
-  static constexpr int TAB_OFF = XFER_OFF + 2 * SLOT_BYTES;
+  static constexpr int MAXR = kMlaTcSetChunk;
+  static constexpr int TAB_OFF = XFER_OFF + NSLOT * SLOT_BYTES;
   static constexpr int TAB_BYTES = (4 * MAXR + 4) * 4;
   static constexpr int BAR_OFF = TAB_OFF + TAB_BYTES;
   static constexpr int NBAR = 40;
   static constexpr int SMEM = 1024 + BAR_OFF + NBAR * 8;
-  static constexpr int THREADS = 256;
+  static constexpr int THREADS = 320;
+  static constexpr int W_MMA = 8, W_XFER = 9;           // warps 0-3 producers, 4-7 softmax / correction
   static constexpr int MIN_BLOCKS = TBLK;               // a share holds at least one tile
   static constexpr int PART = DV + 4;                   // partial row: 512 floats, then the LSE
   static constexpr uint32_t IDESC_S = tc::idesc_bf16(128, NK, 0, 0);
-  static constexpr uint32_t IDESC_PV = tc::idesc_bf16(128, 128, 0, 1);
+  static constexpr uint32_t IDESC_PV = tc::idesc_bf16(128, 256, 0, 1);
   static constexpr uint32_t QCOL = 0, SCOL = 288;       // TMEM (CTA 0): Q, then S buffers 0 and 1
 };
 static_assert(MtCfg::XFER_BYTES % 16 == 0 && MtCfg::XFER_BYTES <= MtCfg::SLOT_BYTES, "bulk copy size");
@@ -92,14 +103,14 @@ enum MtBar {
   B_S_FULL = 16,      // [2] CTA 0: S buffer written
   B_S_FREE = 18,      // [2] CTA 0: S buffer read into registers (128 arrivals)
   B_Q_FULL = 20,      // CTA 0: the piece's Q is in tensor memory (128 arrivals)
-  B_STG_FULL = 21,    // [2] CTA 0: staging buffer written (128 arrivals)
-  B_P_FREE = 23,      // [2] CTA 0: CTA 1's slot may be refilled (1 commit + 4 warp arrivals)
-  B_P_FULL = 25,      // [2] CTA 1: the slot's bulk copy landed
-  B_O_READY = 27,     // CTA 1: the products before a rescale are done
-  B_O_FIXED = 28,     // CTA 1: O rescaled (128 arrivals)
-  B_O_FULL = 29,      // CTA 1: the piece's last product is done
-  B_O_EMPTY = 30,     // CTA 1: O read out (128 arrivals)
-  B_FIN = 31,         // every product of this CTA is done
+  B_STG_FULL = 21,    // [3] CTA 0: staging buffer written (128 arrivals)
+  B_P_FREE = 24,      // [3] CTA 0: CTA 1's slot may be refilled (1 commit + 4 warp arrivals)
+  B_P_FULL = 27,      // [3] CTA 1: the slot's bulk copy landed
+  B_O_READY = 30,     // CTA 1: the products before a rescale are done
+  B_O_FIXED = 31,     // CTA 1: O rescaled (128 arrivals)
+  B_O_FULL = 32,      // CTA 1: the piece's last product is done
+  B_O_EMPTY = 33,     // CTA 1: O read out (128 arrivals)
+  B_FIN = 34,         // every product of this CTA is done
 };
 
 // ---- cluster helpers ----------------------------------------------------------------------------
@@ -114,19 +125,11 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
+// Arrive on a barrier in another CTA of the cluster (the consumer's release of a slot its peer
+// refills). Waits on such barriers, and on barriers completed by a peer's bulk copy, are
+// CTA-scope like those on TMA loads: a cluster-scope acquire per probe costs hundreds of clocks.
 __device__ __forceinline__ void remote_arrive(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Bulk copy of `bytes` from this CTA's shared memory into the peer's, counted on the peer's
 // barrier.
@@ -163,15 +166,12 @@ __device__ __forceinline__ void touch_regs(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// Bounded wait (CTA-local abort flag, as in the other kernels); `cluster` = the barrier is
-// completed from the peer CTA (acquire at cluster scope).
-template <bool CLUSTER>
+// Bounded wait (CTA-local abort flag, as in the other kernels).
 __device__ __forceinline__ bool mt_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* err) {
-  auto probe = [&]() { return CLUSTER ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (probe()) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (probe()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -182,10 +182,9 @@ __device__ __forceinline__ bool mt_wait(uint64_t* bar, uint32_t parity, volatile
     }
   }
 }
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool mt_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned int* err) {
-  return __all_sync(0xffffffffu, mt_wait<CLUSTER>(bar, parity, abort_flag, err));
+  return __all_sync(0xffffffffu, mt_wait(bar, parity, abort_flag, err));
 }
 
 // The tiles of a share in order: the pieces of [b0, b1) (one per sequence it touches), each cut
@@ -221,6 +220,43 @@ struct TileWalk {
   // 0 for the others (the first piece of theirs)
   __device__ int slot() const { return pc.lo > 0 ? 0 : 1; }
 };
+
+// This launch's chunk of the request set (kMlaTcSetChunk positions from set_offset), as
+// resolve_set does for the other decode kernels' chunk size.
+__device__ __forceinline__ void mt_resolve_set(const DecodeParams& p, int& begin, int& n) {
+  begin = 0;
+  n = p.max_reqs;
+  if (p.bounds != nullptr) {
+    begin = p.bounds[p.cls];
+    n = min(p.bounds[p.cls + 1] - begin, p.max_reqs);
+    if (n < 0) n = 0;
+  }
+  begin += p.set_offset;
+  n = max(0, min(n - p.set_offset, kMlaTcSetChunk));
+}
+
+// The chunk's sequences into shared memory (scan_set) with the set checks, and out = 0,
+// lse = -inf for sequences with no context (cluster 0's first CTA), as load_set does.
+__device__ __forceinline__ int64_t mt_load_set(const DecodeParams& p, int begin, int n, int* s_pre, int* s_ctx,
+                                               int* s_r, int* s_row, int* s_scan) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  if (blockIdx.x == 0 && tid == 0 && p.bounds != nullptr && p.bounds[p.cls + 1] - p.bounds[p.cls] > p.max_reqs)
+    flag_error(p.err, PKV_DEVERR_REQS);
+  const int cap = min(p.max_seq_len, p.max_blocks * MtCfg::BS);
+  const int64_t total = scan_set<MtCfg::BS>(p.order, p.seq_lens, p.cu_q, begin, n, p.batch_reqs, cap, p.err, s_pre,
+                                            s_ctx, s_r, s_row, s_scan);
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < n; i += nthreads) {
+      if (s_ctx[i] != 0 || s_r[i] < 0) continue;
+      const int64_t row = s_row[i];
+      uint4* dst = reinterpret_cast<uint4*>(p.out + row * MtCfg::H * MtCfg::DV);
+      for (int c16 = 0; c16 < MtCfg::H * MtCfg::DV / 8; ++c16) dst[c16] = make_uint4(0, 0, 0, 0);
+      if (p.lse)
+        for (int h = 0; h < MtCfg::H; ++h) p.lse[row * MtCfg::H + h] = -CUDART_INF_F;
+    }
+  }
+  return total;
+}
 
 // Physical block of table entry `blk0 + lane` (lanes < nbl), read ahead of its use.
 __device__ __forceinline__ int table_entry(const DecodeParams& p, const int* s_r, const TileWalk& w, int lane) {
@@ -284,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
   __shared__ int s_scan[C::THREADS / 32];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ uint32_t s_issued, s_used;  // ring stages the producer issued / the MMA warp consumed
+  __shared__ uint32_t s_issued[MtCfg::NPROD], s_used;  // ring loads each producer issued / the MMA warp consumed
 
   pdl_wait();
   pdl_release();
@@ -295,13 +331,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
   if (rank == 0 && tid == 0) meta[c] = 0ull;  // no cut sequence starts here (until found)
   if (tid == 0) {
     s_abort = 0;
-    s_issued = s_used = 0;
+    for (int i = 0; i < C::NPROD; ++i) s_issued[i] = 0;
+    s_used = 0;
   }
 
   // ---- the set's sequences and their block counts (every CTA, redundantly) ----
   int begin, n;
-  resolve_set(p, begin, n);
-  const int64_t TB = load_set<C::MAXR, C::BS>(p, begin, n, s_pre, s_ctx, s_r, s_row, s_scan);
+  mt_resolve_set(p, begin, n);
+  const int64_t TB = mt_load_set(p, begin, n, s_pre, s_ctx, s_r, s_row, s_scan);
   if (TB == 0) return;  // cluster-uniform: both CTAs return before any cross-CTA access
   const int nsh = active_shares(TB, gridDim.x >> 1, C::MIN_BLOCKS);
   const Shares sh(TB, nsh);
@@ -312,21 +349,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t count = 1;
-      if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_STG_FULL || i == B_STG_FULL + 1 || i == B_Q_FULL ||
+      if (i == B_S_FREE || i == B_S_FREE + 1 || (i >= B_STG_FULL && i < B_STG_FULL + C::NSLOT) || i == B_Q_FULL ||
           i == B_O_FIXED || i == B_O_EMPTY)
         count = 128;  // the four softmax (CTA 0) or correction (CTA 1) warps
-      else if (i == B_P_FREE || i == B_P_FREE + 1)
+      else if (i >= B_P_FREE && i < B_P_FREE + C::NSLOT)
         count = 5;    // CTA 1's commit and its four correction warps
+      else if (rank == 1 && i >= B_RING_FULL && i < B_RING_FULL + C::NSV)
+        count = C::NPROD;  // a value stage is loaded by all four producer warps
       mbar_init(&bar[i], count);
     }
     fence_mbar_init();
-    if (rank == 1) {  // CTA 1 expects the first two P tiles
-      mbar_arrive_expect_tx(&bar[B_P_FULL], C::XFER_BYTES);
-      mbar_arrive_expect_tx(&bar[B_P_FULL + 1], C::XFER_BYTES);
-    }
+    if (rank == 1)  // CTA 1 expects the first NSLOT P tiles
+      for (int i = 0; i < C::NSLOT; ++i) mbar_arrive_expect_tx(&bar[B_P_FULL + i], C::XFER_BYTES);
     tma_prefetch_desc(&tm);
   }
-  if (warp == 1) tc::tmem_alloc(&s_tmem, 512);
+  if (warp == C::W_MMA) tc::tmem_alloc(&s_tmem, 512);
   tc::fence_before_sync();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers exist before any signal crosses
@@ -334,95 +371,123 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
   const uint32_t tmem = s_tmem;
 
   if (rank == 0) {
-    if (warp == 0) {
-      // ======================= CTA 0: TMA producer of score chunks =======================
-      TileWalk w;
+    if (warp < C::NPROD) {
+      // ======================= CTA 0: TMA producers of score chunks =======================
+      // Chunk kc of the share (tile kc / 9, dims 64 (kc % 9) ..) goes to ring stage kc % NSK.
+      // Stages 2q and 2q + 1 form pair q, freed by one commit and loaded by warp q with one TMA
+      // instruction: lanes 0-6 the 7 blocks of the pair's first chunk, lanes 7-13 those of its
+      // second (which may open the next tile). A warp's TMA instructions complete one after
+      // another, so the boxes per instruction and the four warps side by side set the rate.
+      const int jl = lane % C::TBLK, half = lane / C::TBLK;  // half 2+: idle lanes
+      TileWalk w;                                              // the tile of the pair's first chunk
       w.start(s_pre, n, b0, b1);
-      uint32_t kc = 0;
-      bool ok = true;
-      int blk = checked_block(p, table_entry(p, s_r, w, lane));
-      while (ok) {
-        TileWalk wn = w;
-        const bool more = wn.advance();
-        const int blk_next = more ? table_entry(p, s_r, wn, lane) : 0;  // read ahead
-        const int nbl = w.nbl();
-        for (int ch = 0; ch < C::KCH; ++ch, ++kc) {
-          const int st = kc % C::NSK;
-          const uint32_t use = kc / C::NSK;
-          if (use > 0 && !mt_wait_warp(&bar[B_RING_EMPTY + st], (use - 1) & 1, &s_abort, p.err)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(&bar[B_RING_FULL + st], nbl * 2048);
-          __syncwarp();
-          if (lane < nbl) tma_load_4d(ring + st * C::CH_BYTES + lane * 2048, &tm, &bar[B_RING_FULL + st], 0, ch, 0, blk);
+      uint32_t tw = 0;
+      TileWalk wn = w;
+      bool wn_ok = wn.advance();
+      int e_cur = half < 2 ? table_entry(p, s_r, w, jl) : 0;
+      int e_nxt = half < 2 && wn_ok ? table_entry(p, s_r, wn, jl) : 0;
+      uint32_t last = 0;
+      for (uint32_t u = 0;; ++u) {
+        const uint32_t kc = u * C::NSK + 2 * warp;
+        while (w.have && tw < kc / C::KCH) {  // at most one step: pairs of a warp are 8 chunks apart
+          w = wn;
+          e_cur = e_nxt;
+          ++tw;
+          wn_ok = w.have && wn.advance();
+          e_nxt = half < 2 && wn_ok ? table_entry(p, s_r, wn, jl) : 0;
         }
-        if (!more) break;
-        w = wn;
-        blk = checked_block(p, blk_next);
+        if (!w.have) break;
+        if (u > 0 && !mt_wait_warp(&bar[B_RING_EMPTY + warp], (u - 1) & 1, &s_abort, p.err)) break;
+        const bool second_here = (kc + 1) / C::KCH == tw;
+        const int nbl0 = w.nbl(), nbl1 = second_here ? w.nbl() : (wn_ok ? wn.nbl() : 0);
+        if (lane == 0) mbar_arrive_expect_tx(&bar[B_RING_FULL + 2 * warp], nbl0 * 2048);
+        if (lane == C::TBLK && nbl1 > 0) mbar_arrive_expect_tx(&bar[B_RING_FULL + 2 * warp + 1], nbl1 * 2048);
+        __syncwarp();
+        if (half < 2) {
+          const uint32_t x = kc + half;
+          const bool in_w = x / C::KCH == tw;
+          if (jl < (in_w ? nbl0 : nbl1)) {
+            const int blk = checked_block(p, in_w ? e_cur : e_nxt);
+            tma_load_4d(ring + (2 * warp + half) * C::CH_BYTES + jl * 2048, &tm, &bar[B_RING_FULL + 2 * warp + half], 0,
+                        x % C::KCH, 0, blk);
+          }
+        }
+        last = kc + (nbl1 > 0 ? 2 : 1);
       }
-      if (lane == 0) s_issued = kc;
-    } else if (warp == 1) {
+      if (lane == 0) s_issued[warp] = last;
+    } else if (warp == C::W_MMA) {
       // ======================= CTA 0: MMA issuer, S = Q C^T =======================
-      TileWalk w;
-      w.start(s_pre, n, b0, b1);
-      uint32_t kc = 0, t = 0, pcn = 0;
-      bool ok = true;
-      const uint32_t ring_a = smem_u32(ring);
-      for (; w.have && ok; w.advance(), ++t) {
-        if (w.first()) {
-          if (!mt_wait_warp(&bar[B_Q_FULL], pcn & 1, &s_abort, p.err)) break;
-          ++pcn;
-        }
-        const int sb = t & 1;
-        if (t >= 2 && !mt_wait_warp(&bar[B_S_FREE + sb], ((t >> 1) - 1) & 1, &s_abort, p.err)) break;
-        tc::fence_after_sync();
-        const uint32_t d = tmem + C::SCOL + sb * C::NK;
-        for (int ch = 0; ch < C::KCH; ++ch, ++kc) {
-          const int st = kc % C::NSK;
-          if (!mt_wait_warp(&bar[B_RING_FULL + st], (kc / C::NSK) & 1, &s_abort, p.err)) {
-            ok = false;
-            break;
+      // One thread runs the loop (no warp-wide vote per chunk: the issue overhead per chunk is
+      // what bounds this role); a commit frees a pair of ring stages.
+      if (lane == 0) {
+        TileWalk w;
+        w.start(s_pre, n, b0, b1);
+        uint32_t kc = 0, t = 0, pcn = 0;
+        bool ok = true;
+        const uint32_t ring_a = smem_u32(ring);
+        for (; w.have && ok; w.advance(), ++t) {
+          if (w.first()) {
+            if (!mt_wait(&bar[B_Q_FULL], pcn & 1, &s_abort, p.err)) break;
+            ++pcn;
           }
+          const int sb = t & 1;
+          if (t >= 2 && !mt_wait(&bar[B_S_FREE + sb], ((t >> 1) - 1) & 1, &s_abort, p.err)) break;
           tc::fence_after_sync();
-          if (lane == 0) {
+          const uint32_t d = tmem + C::SCOL + sb * C::NK;
+          for (int ch = 0; ch < C::KCH; ++ch, ++kc) {
+            const int st = kc % C::NSK;
+            if (!mt_wait(&bar[B_RING_FULL + st], (kc / C::NSK) & 1, &s_abort, p.err)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
             const uint32_t kb = ring_a + st * C::CH_BYTES;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               tc::mma_ts(d, tmem + C::QCOL + (ch * 4 + kk) * 8, tc::smem_desc(kb + kk * 32, 16, 1024), C::IDESC_S,
                          (ch | kk) != 0);
-            tc::commit(&bar[B_RING_EMPTY + st]);
+            if (kc & 1) tc::commit(&bar[B_RING_EMPTY + (kc >> 1) % (C::NSK / 2)]);
           }
-          __syncwarp();
+          if (!ok) break;
+          tc::commit(&bar[B_S_FULL + sb]);
         }
-        if (!ok) break;
-        if (lane == 0) tc::commit(&bar[B_S_FULL + sb]);
-        __syncwarp();
-      }
-      if (lane == 0) {
         s_used = kc;
         tc::commit(&bar[B_FIN]);
+        mt_wait(&bar[B_FIN], 0, &s_abort, p.err);
       }
       __syncwarp();
-      mt_wait_warp(&bar[B_FIN], 0, &s_abort, p.err);
-    } else if (warp == 2) {
+    } else if (warp == C::W_XFER) {
       // ======================= CTA 0: sends staged P tiles to CTA 1 =======================
       TileWalk w;
       w.start(s_pre, n, b0, b1);
       uint32_t t = 0;
       for (; w.have; w.advance(), ++t) {
-        const int pb = t & 1;
-        if (!mt_wait_warp(&bar[B_STG_FULL + pb], (t >> 1) & 1, &s_abort, p.err)) break;
+        const int pb = t % C::NSLOT;
+        if (!mt_wait_warp(&bar[B_STG_FULL + pb], (t / C::NSLOT) & 1, &s_abort, p.err)) break;
         if (lane == 0) {
           const uint32_t src = smem_u32(xfer + pb * C::SLOT_BYTES);
           copy_to_peer(peer_addr(src, 1), src, C::XFER_BYTES, peer_addr(smem_u32(&bar[B_P_FULL + pb]), 1));
         }
         __syncwarp();
       }
-      // CTA 1 signals p_free of every tile; the last two signals must land before this CTA exits
-      for (uint32_t u = t >= 2 ? t - 2 : 0; u < t; ++u)
-        if (!mt_wait_warp<true>(&bar[B_P_FREE + (u & 1)], (u >> 1) & 1, &s_abort, p.err)) break;
-    } else if (warp >= 4) {
+      // CTA 1 signals p_free of every tile; the last NSLOT signals must land before this CTA exits
+      for (uint32_t u = t >= C::NSLOT ? t - C::NSLOT : 0; u < t; ++u)
+        if (!mt_wait_warp(&bar[B_P_FREE + u % C::NSLOT], (u / C::NSLOT) & 1, &s_abort, p.err)) break;
+      if (lane == 0) {
+        // the merge kernel learns of the cut sequence that starts in this share, if any: the
+        // share's last piece begins its sequence and ends before it
+        TileWalk wl;
+        wl.start(s_pre, n, b0, b1);
+        Piece last = wl.pc;
+        while (wl.it.next(last)) {
+        }
+        const int nb = (s_ctx[last.i] + C::BS - 1) / C::BS;
+        if (last.lo == 0 && last.hi < nb) {
+          const int np = sh.of(s_pre[last.i + 1] - 1) - c + 1;
+          meta[c] = (static_cast<unsigned long long>(np) << 32) | static_cast<uint32_t>(s_row[last.i]);
+        }
+      }
+    } else if (warp >= 4 && warp < 8) {
       // ======================= CTA 0: softmax =======================
       const int h = (warp & 3) * 32 + lane;  // head = TMEM lane
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -492,9 +557,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
           resc = true;
         }
         const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
-        // CTA 1's slot for this staging buffer is free once the P V two tiles back is done
-        const int pb = t & 1;
-        if (t >= 2 && !mt_wait_warp<true>(&bar[B_P_FREE + pb], ((t >> 1) - 1) & 1, &s_abort, p.err)) break;
+        // CTA 1's slot for this staging buffer is free once the P V NSLOT tiles back is done
+        const int pb = t % C::NSLOT;
+        if (t >= C::NSLOT && !mt_wait_warp(&bar[B_P_FREE + pb], (t / C::NSLOT - 1) & 1, &s_abort, p.err))
+          break;
         uint8_t* stg = xfer + pb * C::SLOT_BYTES;
         const uint32_t stg_a = smem_u32(stg);
         float rs = 0.f;
@@ -529,26 +595,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bar[B_STG_FULL + pb]);
       }
-    } else if (warp == 3 && lane == 0) {
-      // the merge kernel learns of the cut sequence that starts in this share, if any: the
-      // share's last piece begins its sequence and ends before it
-      TileWalk w;
-      w.start(s_pre, n, b0, b1);
-      Piece last = w.pc;
-      while (w.it.next(last)) {
-      }
-      const int nb = (s_ctx[last.i] + C::BS - 1) / C::BS;
-      if (last.lo == 0 && last.hi < nb) {
-        const int np = sh.of(s_pre[last.i + 1] - 1) - c + 1;
-        meta[c] = (static_cast<unsigned long long>(np) << 32) | static_cast<uint32_t>(s_row[last.i]);
-      }
     }
   } else {
-    if (warp == 0) {
-      // ======================= CTA 1: TMA producer of value stages =======================
+    if (warp < C::NPROD) {
+      // ======================= CTA 1: TMA producers of value stages =======================
+      // Stage j of a tile holds value dims 256 j .. 256 j + 255 (chunks 4 j .. 4 j + 3); warp q
+      // loads chunk 4 j + q of every stage, so the four warps' TMA instructions run side by side.
       TileWalk w;
       w.start(s_pre, n, b0, b1);
-      uint32_t vc = 0;
+      uint32_t vc = 0, last = 0;
       bool ok = true;
       int blk = checked_block(p, table_entry(p, s_r, w, lane));
       while (ok) {
@@ -556,27 +611,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
         const bool more = wn.advance();
         const int blk_next = more ? table_entry(p, s_r, wn, lane) : 0;
         const int nbl = w.nbl();
-        for (int vs = 0; vs < 4; ++vs, ++vc) {
+        for (int j = 0; j < 2; ++j, ++vc) {
           const int st = vc % C::NSV;
           const uint32_t use = vc / C::NSV;
           if (use > 0 && !mt_wait_warp(&bar[B_RING_EMPTY + st], (use - 1) & 1, &s_abort, p.err)) {
             ok = false;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(&bar[B_RING_FULL + st], nbl * 4096);
+          if (lane == 0) mbar_arrive_expect_tx(&bar[B_RING_FULL + st], nbl * 2048);
           __syncwarp();
-          if (lane < nbl) {
-            uint8_t* dst = ring + st * C::VST_BYTES + lane * 2048;
-            tma_load_4d(dst, &tm, &bar[B_RING_FULL + st], 0, 2 * vs, 0, blk);
-            tma_load_4d(dst + C::CH_BYTES, &tm, &bar[B_RING_FULL + st], 0, 2 * vs + 1, 0, blk);
-          }
+          if (lane < nbl)
+            tma_load_4d(ring + st * C::VST_BYTES + warp * C::CH_BYTES + lane * 2048, &tm, &bar[B_RING_FULL + st], 0,
+                        4 * j + warp, 0, blk);
+          last = vc + 1;
         }
         if (!more) break;
         w = wn;
         blk = checked_block(p, blk_next);
       }
-      if (lane == 0) s_issued = vc;
-    } else if (warp == 1) {
+      if (lane == 0) s_issued[warp] = last;
+    } else if (warp == C::W_MMA) {
       // ======================= CTA 1: MMA issuer, O += P V =======================
       TileWalk w;
       w.start(s_pre, n, b0, b1);
@@ -584,8 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
       bool ok = true;
       const uint32_t ring_a = smem_u32(ring);
       for (; w.have && ok; w.advance(), ++t) {
-        const int ps = t & 1;
-        if (!mt_wait_warp<true>(&bar[B_P_FULL + ps], (t >> 1) & 1, &s_abort, p.err)) break;
+        const int ps = t % C::NSLOT;
+        if (!mt_wait_warp(&bar[B_P_FULL + ps], (t / C::NSLOT) & 1, &s_abort, p.err)) break;
         const uint8_t* slot = xfer + ps * C::SLOT_BYTES;
         const int* fl = reinterpret_cast<const int*>(slot + C::TR_FLAGS);
         const bool any = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
@@ -600,7 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
         tc::fence_after_sync();
         const int valid = w.valid(s_ctx);
         const uint32_t pa = smem_u32(slot);
-        for (int vs = 0; vs < 4; ++vs, ++vc) {
+        for (int j = 0; j < 2; ++j, ++vc) {
           const int st = vc % C::NSV;
           if (!mt_wait_warp(&bar[B_RING_FULL + st], (vc / C::NSV) & 1, &s_abort, p.err)) {
             ok = false;
@@ -610,8 +664,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
           if (valid < C::NK) {
             // keys past the context end (or past the piece's last loaded block): zero their V
             // rows so that P = 0 there never meets a non-finite value
-            for (int e = lane; e < (C::NK - valid) * 16; e += 32) {
-              const int rrow = valid + (e >> 4), rest = e & 15;
+            for (int e = lane; e < (C::NK - valid) * 32; e += 32) {
+              const int rrow = valid + (e >> 5), rest = e & 31;
               *reinterpret_cast<uint4*>(vb + (rest >> 3) * C::CH_BYTES + rrow * 128 + (rest & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -623,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
             const uint32_t va = ring_a + st * C::VST_BYTES;
 #pragma unroll
             for (int kk = 0; kk < C::NK / 16; ++kk)
-              tc::mma_ss(tmem + vs * 128, tc::smem_desc(pa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+              tc::mma_ss(tmem + j * 256, tc::smem_desc(pa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                          tc::smem_desc(va + kk * 2048, C::CH_BYTES, 1024), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
             tc::commit(&bar[B_RING_EMPTY + st]);
           }
@@ -644,7 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
       }
       __syncwarp();
       mt_wait_warp(&bar[B_FIN], 0, &s_abort, p.err);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
       // ======================= CTA 1: correction and epilogue =======================
       const int h = (warp & 3) * 32 + lane;  // O row = TMEM lane
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -653,8 +707,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
       w.start(s_pre, n, b0, b1);
       uint32_t t = 0, pcn = 0, rc = 0;
       for (; w.have; w.advance(), ++t) {
-        const int ps = t & 1;
-        if (!mt_wait_warp<true>(&bar[B_P_FULL + ps], (t >> 1) & 1, &s_abort, p.err)) break;
+        const int ps = t % C::NSLOT;
+        if (!mt_wait_warp(&bar[B_P_FULL + ps], (t / C::NSLOT) & 1, &s_abort, p.err)) break;
         const uint8_t* slot = xfer + ps * C::SLOT_BYTES;
         const int* fl = reinterpret_cast<const int*>(slot + C::TR_FLAGS);
         const bool any = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
@@ -722,12 +776,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
   // ---- teardown: loads still in flight (after an abort) land before the CTA exits ----
   tc::fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
+  if (warp < C::NPROD && lane == 0) {
+    // a producer's loads not yet consumed (only after an abort): its own stages, in order
     const int ns = rank == 0 ? C::NSK : C::NSV;
-    for (uint32_t i = s_used; i < s_issued; ++i)
+    for (uint32_t i = s_used; i < s_issued[warp]; ++i) {
+      if (rank == 0 && (i % ns) / 2 != static_cast<uint32_t>(warp)) continue;
       if (!mbar_wait(&bar[B_RING_FULL + i % ns], (i / ns) & 1, p.err)) break;
+    }
   }
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }

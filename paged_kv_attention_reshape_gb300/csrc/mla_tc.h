@@ -10,6 +10,10 @@
 
 namespace pkv {
 
+// Requests one launch of the 128-head kernel holds (its shared memory goes to the rings and the P
+// slots): a larger set takes consecutive launches over set positions [k * 256, (k + 1) * 256).
+constexpr int kMlaTcSetChunk = 256;
+
 // Workspace of the 128-head kernel: per cluster share, two partial slots of 128 rows x (512
 // output dims + LSE) floats (the pieces of cut sequences), then one 64-bit merge record per
 // share. p.ws_part points at the partials, p.ws_ctr at the records (mla_tc_meta_offset bytes in).

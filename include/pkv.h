@@ -251,6 +251,11 @@ pkv_status pkv_paged_decode_attn_noalloc(const void* q, pkv_cache cache,
  * behave as in paged_decode_attn; the workspace size comes from
  * pkv_mla_decode_workspace_size with the same num_q_heads. Other shapes return
  * PKV_ERR_UNSUPPORTED.
+ * Kernels: up to 64 query heads run on warp-level MMA, 16 heads a CTA; at 128 heads (the layer
+ * without tensor parallelism) a tcgen05 kernel runs on clusters of two CTAs (scores on one
+ * SM, O += P V in the other's tensor memory), followed by a small kernel that merges the
+ * pieces of sequences cut at share edges (two launches per 256 requests of the set; about
+ * 40 MB of workspace, the partials of two pieces per cluster).
  * ------------------------------------------------------------------------------------- */
 size_t pkv_mla_decode_workspace_size(int32_t max_reqs, int32_t num_q_heads, int32_t max_seq_len);
 pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* block_tables,

@@ -288,8 +288,9 @@ def extend_attn(q, k_new, v_new, cu_q, seq_lens, k_cache, v_cache, block_tables,
                 max_seq_len, reqs: Optional[Reqs] = None, chunk_budget_tokens=32768, scale=None,
                 out=None, lse=None, stream=None, k_scale=1.0, v_scale=1.0, workspace=None):
     """New tokens attend to their cached context (paged) and causally to themselves. An FP8
-    cache (uint8 / float8 codes with per-tensor scales) is gathered into a bf16 workspace of
-    the set's context first (allocated here when not given)."""
+    cache (uint8 / float8 codes with per-tensor scales) is read as codes and converted in the
+    kernel at head_dim 128; at head_dim 64 it is gathered into a bf16 workspace of the set's
+    context first (allocated here when not given)."""
     lib = _lib.load()
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
         _need(t, torch.bfloat16, n)

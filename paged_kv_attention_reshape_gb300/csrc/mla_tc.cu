@@ -49,6 +49,7 @@
 #include "decode_shares.cuh"
 #include "launch.h"
 #include "mla_tc.h"
+#include "softmax.cuh"
 #include "tc.cuh"
 
 namespace pkv {
@@ -540,10 +541,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
         tc::fence_before_sync();
         mbar_arrive(&bar[B_S_FREE + sb]);
         const int valid = w.valid(s_ctx);
+        const bool full = valid == C::NK;  // tile-uniform
         float mx = -CUDART_INF_F;
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < C::NK; ++e)
-          if (e < valid) mx = fmaxf(mx, __uint_as_float(v[e]));
+          for (int e = 0; e < C::NK; e += 2) mx = sm::max3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < C::NK; ++e)
+            if (e < valid) mx = fmaxf(mx, __uint_as_float(v[e]));
+        }
         mx *= sl;
         float alpha = 1.f;
         bool resc = false;
@@ -564,20 +571,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
         uint8_t* stg = xfer + pb * C::SLOT_BYTES;
         const uint32_t stg_a = smem_u32(stg);
         float rs = 0.f;
+        if (full) {
+          // every column valid: pairs of columns in packed fp32 (one instruction per pair for
+          // the scale-and-shift and for the running sum)
+          const uint64_t sl2 = sm::f2(sl, sl), nm2 = sm::f2(neg_m, neg_m);
+          uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < C::NK / 8; ++u) {
-          uint32_t pk[4];
+          for (int u = 0; u < C::NK / 8; ++u) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int e0 = u * 8 + 2 * j;
-            const float x0 = fmaf(__uint_as_float(v[e0]), sl, neg_m);
-            const float x1 = fmaf(__uint_as_float(v[e0 + 1]), sl, neg_m);
-            const float p0 = e0 < valid ? ex2_approx(x0) : 0.f;
-            const float p1 = e0 + 1 < valid ? ex2_approx(x1) : 0.f;
-            rs += p0 + p1;
-            pk[j] = pack_bf16(p0, p1);
+            for (int j = 0; j < 4; ++j) {
+              const int e0 = u * 8 + 2 * j;
+              const uint64_t x = sm::fma2(sm::f2(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1])), sl2, nm2);
+              float x0, x1;
+              sm::unf2(x, x0, x1);
+              const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
+              rs2 = sm::add2(rs2, pp);
+              pk[j] = sm::bf16x2(pp);
+            }
+            st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7), make_uint4(pk[0], pk[1], pk[2], pk[3]));
           }
-          st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          float r0, r1;
+          sm::unf2(rs2, r0, r1);
+          rs = r0 + r1;
+        } else {
+#pragma unroll
+          for (int u = 0; u < C::NK / 8; ++u) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e0 = u * 8 + 2 * j;
+              const float x0 = fmaf(__uint_as_float(v[e0]), sl, neg_m);
+              const float x1 = fmaf(__uint_as_float(v[e0 + 1]), sl, neg_m);
+              const float p0 = e0 < valid ? ex2_approx(x0) : 0.f;
+              const float p1 = e0 + 1 < valid ? ex2_approx(x1) : 0.f;
+              rs += p0 + p1;
+              pk[j] = pack_bf16(p0, p1);
+            }
+            st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          }
         }
         l += rs;
         reinterpret_cast<float*>(stg + C::TR_ALPHA)[h] = alpha;

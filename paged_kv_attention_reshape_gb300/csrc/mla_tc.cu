@@ -564,12 +564,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
           resc = true;
         }
         const float neg_m = m == -CUDART_INF_F ? 0.f : -m;
-        // CTA 1's slot for this staging buffer is free once the P V NSLOT tiles back is done
-        const int pb = t % C::NSLOT;
-        if (t >= C::NSLOT && !mt_wait_warp(&bar[B_P_FREE + pb], (t / C::NSLOT - 1) & 1, &s_abort, p.err))
-          break;
-        uint8_t* stg = xfer + pb * C::SLOT_BYTES;
-        const uint32_t stg_a = smem_u32(stg);
+        // P (bf16 pairs) into registers first, so that the wait for the staging buffer overlaps
+        // the exponentials
+        uint32_t pk[C::NK / 2];
         float rs = 0.f;
         if (full) {
           // every column valid: pairs of columns in packed fp32 (one instruction per pair for
@@ -577,40 +574,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MtCfg::THREADS, 1)
           const uint64_t sl2 = sm::f2(sl, sl), nm2 = sm::f2(neg_m, neg_m);
           uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
-          for (int u = 0; u < C::NK / 8; ++u) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int e0 = u * 8 + 2 * j;
-              const uint64_t x = sm::fma2(sm::f2(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1])), sl2, nm2);
-              float x0, x1;
-              sm::unf2(x, x0, x1);
-              const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
-              rs2 = sm::add2(rs2, pp);
-              pk[j] = sm::bf16x2(pp);
-            }
-            st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          for (int e2 = 0; e2 < C::NK / 2; ++e2) {
+            const uint64_t x = sm::fma2(sm::f2(__uint_as_float(v[2 * e2]), __uint_as_float(v[2 * e2 + 1])), sl2, nm2);
+            float x0, x1;
+            sm::unf2(x, x0, x1);
+            const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
+            rs2 = sm::add2(rs2, pp);
+            pk[e2] = sm::bf16x2(pp);
           }
           float r0, r1;
           sm::unf2(rs2, r0, r1);
           rs = r0 + r1;
         } else {
 #pragma unroll
-          for (int u = 0; u < C::NK / 8; ++u) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int e0 = u * 8 + 2 * j;
-              const float x0 = fmaf(__uint_as_float(v[e0]), sl, neg_m);
-              const float x1 = fmaf(__uint_as_float(v[e0 + 1]), sl, neg_m);
-              const float p0 = e0 < valid ? ex2_approx(x0) : 0.f;
-              const float p1 = e0 + 1 < valid ? ex2_approx(x1) : 0.f;
-              rs += p0 + p1;
-              pk[j] = pack_bf16(p0, p1);
-            }
-            st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          for (int e2 = 0; e2 < C::NK / 2; ++e2) {
+            const int e0 = 2 * e2;
+            const float x0 = fmaf(__uint_as_float(v[e0]), sl, neg_m);
+            const float x1 = fmaf(__uint_as_float(v[e0 + 1]), sl, neg_m);
+            const float p0 = e0 < valid ? ex2_approx(x0) : 0.f;
+            const float p1 = e0 + 1 < valid ? ex2_approx(x1) : 0.f;
+            rs += p0 + p1;
+            pk[e2] = pack_bf16(p0, p1);
           }
         }
+        // CTA 1's slot for this staging buffer is free once the P V NSLOT tiles back is done
+        const int pb = t % C::NSLOT;
+        if (t >= C::NSLOT && !mt_wait_warp(&bar[B_P_FREE + pb], (t / C::NSLOT - 1) & 1, &s_abort, p.err))
+          break;
+        uint8_t* stg = xfer + pb * C::SLOT_BYTES;
+        const uint32_t stg_a = smem_u32(stg);
+#pragma unroll
+        for (int u = 0; u < C::NK / 8; ++u)
+          st_shared_v4(stg_a + (u >> 3) * 16384 + sw128(h, u & 7),
+                       make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
         l += rs;
         reinterpret_cast<float*>(stg + C::TR_ALPHA)[h] = alpha;
         const bool wres = __any_sync(0xffffffffu, resc);

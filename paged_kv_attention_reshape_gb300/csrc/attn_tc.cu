@@ -192,6 +192,14 @@ __device__ __forceinline__ int64_t tc_next(int64_t w, int& odd) {
   return w + step;
 }
 
+// Columns n .. 31 of a 32-column chunk of S (raw fp32 bits) become -inf: keys outside the row's
+// range (past the context's end, or after the row in causal order) get p = 0, and whatever the
+// tensor core wrote there (not necessarily finite) never enters the arithmetic.
+__device__ __forceinline__ void mask_cols(uint32_t (&v)[32], int n) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = e < n ? v[e] : 0xFF800000u;
+}
+
 // Bounded wait that also gives up as soon as another role has given up.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         unsigned int* err) {
@@ -582,9 +590,9 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
 #pragma unroll
             for (int e = 0; e < 32; e += 2) mx = sm::max3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
           } else {
+            mask_cols(v, kv - c * 32);
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e < kv) mx = fmaxf(mx, __uint_as_float(v[e]));
+            for (int e = 0; e < 32; e += 2) mx = sm::max3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
           }
         }
         mx = mx * sl;  // -inf stays -inf
@@ -626,23 +634,30 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
         if (full) {
           rs = full_pass();
         } else {
+          // the same packed pairs with the columns past kv at -inf (their p is 0)
+          const uint64_t sc2 = sm::f2(sl, sl), nm2 = sm::f2(neg_m, neg_m);
+          uint64_t rs2 = sm::f2(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
             tc::ld32(srow + c * 32, v);
             tc::wait_ld();
+            mask_cols(v, kv - c * 32);
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl, neg_m));
-              float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl, neg_m));
-              p0 = (c * 32 + e < kv) ? p0 : 0.f;
-              p1 = (c * 32 + e + 1 < kv) ? p1 : 0.f;
-              rs += p0 + p1;
-              pk[e / 2] = C::F16 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+              const uint64_t x = sm::fma2(sm::f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+              float x0, x1;
+              sm::unf2(x, x0, x1);
+              const uint64_t pp = sm::f2(ex2_approx(x0), ex2_approx(x1));
+              rs2 = sm::add2(rs2, pp);
+              pk[e / 2] = C::F16 ? sm::f16x2(pp) : sm::bf16x2(pp);
             }
             tc::st16(srow + c * 16, pk);
           }
+          float r0, r1;
+          sm::unf2(rs2, r0, r1);
+          rs = r0 + r1;
         }
         }
         if (vsc) rs *= p.ctx_v_scale;  // the row sum of the unshifted p

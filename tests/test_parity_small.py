@@ -774,6 +774,33 @@ def test_extend_ragged(pkv, G, D):
 
 
 @pytest.mark.parametrize("D", [64, 128])
+def test_extend_nonfinite_past_the_context_end_is_ignored(pkv, D):
+    """Cache rows after a context's last token (in its last block) may hold anything: NaN and
+    +inf keys and inf values here, with peaked queries. The context's last key tile masks those
+    columns before any arithmetic, and their value rows are zeroed."""
+    Hkv = 2
+    new = [1, 40, 130, 7, 64]
+    ctx = [5, 100, 300, 17, 129]
+    b = gen.extend_batch(new, ctx, Hq=4 * Hkv, Hkv=Hkv, D=D, seed=70 + D, q_scale=3.0)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    bt = b.block_tables.numpy()
+    for r, C in enumerate(ctx):
+        if C % 16:
+            last = bt[r, C // 16]
+            kc[last, C % 16:] = float("nan")
+            kc[last, C % 16::3] = float("inf")
+            vc[last, C % 16:] = float("inf")
+    g = b.to(DEV)
+    scale = default_scale(D)
+    out, lse = pkv.extend_attn(g.q, g.k_new, g.v_new, g.cu_q, g.seq_lens, kc.to(DEV), vc.to(DEV), g.block_tables,
+                               max(new), max(b.seq_lens_list), scale=scale)
+    ref, ref_lse = oracle_extend(b, bits(kc), bits(vc), scale)
+    assert not np.isnan(ref).any()
+    compare_attention(out, lse, ref, ref_lse, what=f"extend nonfinite tail D={D}")
+    assert _errors(pkv) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
 def test_prefill_ragged(pkv, D):
     lens = [1, 17, 64, 65, 200, 128, 3]
     b = gen.prefill_batch(lens, Hq=16, Hkv=4, D=D, seed=D)

@@ -68,6 +68,10 @@
  *   each over the next positions of the set (a launch whose positions lie past the set's
  *   actual size exits at once), so sets of any size up to the call's limit are served in full.
  *
+ * The attention calls take the softmax scale as `scale`. It must be positive and finite, else
+ * the call returns PKV_ERR_INVALID_ARG. The kernels take each row's maximum over the raw
+ * scores, which commutes with a positive scale only.
+ *
  * Supported shapes (anything else returns PKV_ERR_UNSUPPORTED; there is no fallback path):
  *   head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}; block_size 16 for the
  *   attention calls (kv_cache_write and kv_block_pack take any block_size >= 1). The MLA

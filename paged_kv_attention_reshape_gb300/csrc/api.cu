@@ -191,6 +191,9 @@ int max_smem_optin() {
   return cache[d];
 }
 
+// The softmax scale: positive and finite (each row's max is taken over the raw scores).
+static bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
 cudaError_t set_smem_attr_once(const void* func, int bytes, int slot) {
   static std::mutex mu;
   static bool done[kAttrCount][kMaxDevices] = {};
@@ -450,7 +453,7 @@ pkv_status pkv_paged_decode_attn(const void* q, pkv_cache cache, const int32_t* 
   if (st != PKV_OK) return st;
   if ((st = check_reqs(reqs)) != PKV_OK) return st;
   if (!group_ok(num_q_heads, cache.num_kv_heads)) return PKV_ERR_UNSUPPORTED;
-  if (max_blocks <= 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (max_blocks <= 0 || max_seq_len < 0 || !scale_ok(scale)) return PKV_ERR_INVALID_ARG;
   if (reqs.max_reqs == 0) return PKV_OK;
   if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
     return PKV_ERR_INVALID_ARG;
@@ -522,7 +525,7 @@ pkv_status pkv_mla_decode_attn(const void* q, pkv_cache cache, const int32_t* bl
       cache.block_size != 16 || v_dim != 512)
     return PKV_ERR_UNSUPPORTED;
   if (num_q_heads <= 0 || num_q_heads % 16 != 0 || num_q_heads > 128) return PKV_ERR_UNSUPPORTED;
-  if (max_blocks <= 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (max_blocks <= 0 || max_seq_len < 0 || !scale_ok(scale)) return PKV_ERR_INVALID_ARG;
   if (reqs.max_reqs == 0) return PKV_OK;
   if (q == nullptr || out == nullptr || block_tables == nullptr || seq_lens == nullptr)
     return PKV_ERR_INVALID_ARG;
@@ -594,7 +597,7 @@ static pkv_status run_attention(const void* q, const void* k, const void* v, int
     return PKV_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   if (!group_ok(Hq, Hkv)) return PKV_ERR_UNSUPPORTED;
-  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale))
+  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !scale_ok(scale))
     return PKV_ERR_INVALID_ARG;
   if (reqs.max_reqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
   if (num_tokens > INT32_MAX || num_tokens * Hq > INT32_MAX) return PKV_ERR_UNSUPPORTED;
@@ -702,7 +705,7 @@ pkv_status pkv_extend_attn(const void* q, const void* k_new, const void* v_new, 
   const int Hkv = cache.num_kv_heads, D = cache.head_dim;
   if ((D != 64 && D != 128) || cache.block_size != 16) return PKV_ERR_UNSUPPORTED;
   if (!group_ok(num_q_heads, Hkv)) return PKV_ERR_UNSUPPORTED;
-  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 || !scale_ok(scale)) return PKV_ERR_INVALID_ARG;
   if (reqs.max_reqs == 0 || max_q_len == 0 || num_tokens == 0) return PKV_OK;
   if (seq_lens == nullptr || block_tables == nullptr || max_blocks <= 0 || cu_q == nullptr)
     return PKV_ERR_INVALID_ARG;

@@ -91,6 +91,14 @@ def test_host_checks_reject_bad_arguments_without_a_gpu(lib):
     empty = _lib.PkvReqs(None, None, 0, 0, 4)
     assert lib.pkv_varlen_prefill_attn(fake, fake, fake, 8, fake, empty, 4, 2, 128, 8, 1.0, fake,
                                        None, None) == 0
+    # the softmax scale must be positive and finite (checked before the empty-set shortcut)
+    for bad_scale in (0.0, -0.125, float("inf"), float("nan")):
+        assert lib.pkv_varlen_prefill_attn(fake, fake, fake, 8, fake, empty, 4, 2, 128, 8, bad_scale, fake,
+                                           None, None) == 1
+        assert lib.pkv_extend_attn(fake, fake, fake, 8, fake, fake, cache, fake, 4, empty, 4, 8, 100, 0,
+                                   bad_scale, fake, None, None, 0, None) == 1
+        assert lib.pkv_paged_decode_attn(fake, cache, fake, 4, fake, None, empty, 4, 100, bad_scale, fake, None,
+                                         None, 0, None) == 1
 
 
 def test_decode_workspace_query_is_host_only(lib):

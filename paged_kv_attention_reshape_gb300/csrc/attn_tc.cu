@@ -748,9 +748,11 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
     int64_t w_static = blockIdx.x;
     int odd = 0;
     for (uint32_t items = 0; ok; ++items) {
-      // the Q buffer is free (the previous item's S products are done): take the next item and
-      // publish it to the MMA and softmax warps
-      if (items > 0 && !tc_wait_warp(q_empty, (items - 1) & 1, &s_abort, p.err)) break;
+      // bf16 context: take the next item and publish it to the MMA and softmax warps while the
+      // previous item's last S products run, ask L2 for its Q tiles, then load them once the Q
+      // buffer is free (long extend +2 %, the mixed step +1.4 %). The FP8 context takes its
+      // item once the Q buffer is free (the early form measured 2.5 % slower there).
+      if (C::CONV && items > 0 && !tc_wait_warp(q_empty, (items - 1) & 1, &s_abort, p.err)) break;
       long long w;
       if (claim) {
         const int e = static_cast<int>(items % C::ITEM_RING);
@@ -770,6 +772,20 @@ __global__ void __launch_bounds__(TcCfg<D, KIND>::THREADS, 1) attention_tc_kerne
       }
       if (w < 0) break;
       const TcItem it = tc_item(p, s_start, s_req, s_perm, n, w, HP);
+      if (!C::CONV && items > 0 && lane == 0) {
+        if (it.dec) {
+#pragma unroll
+          for (int hf = 0; hf < C::HALVES; ++hf)
+            tma_prefetch_l2_3d(&tm_qf, 0, hf, static_cast<int>(it.row0 * p.Hq + it.h0));
+        } else {
+          for (int sl = 0; sl < it.nslot; ++sl)
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              tma_prefetch_l2_3d(&tm_q, 0, (it.h0 + sl) * C::HALVES + hf, static_cast<int>(it.row0) + it.qr0);
+        }
+      }
+      // the Q buffer is free once the previous item's S products are done
+      if (!C::CONV && items > 0 && !tc_wait_warp(q_empty, (items - 1) & 1, &s_abort, p.err)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, it.nslot * C::TILE_BYTES);
         if (it.dec) {
